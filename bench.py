@@ -1,0 +1,400 @@
+"""Benchmark of the GB300 blocked GEMM library; prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload bf16_8192|bf16_4096|tf32_4096|exact_4096|bf16_skinny]
+
+A step is one C = A @ B over one batch of seeded synthetic inputs already resident
+in HBM. Default workload: bf16 M = N = K = 8192, A row-major, B column-major,
+values N(0, 1)/sqrt(K), fp32 accumulation, bf16 output. Inputs total 256 MB per
+step (larger than the 129 MB L2) and rotate over three buffer sets.
+
+``value`` is whole-job TFLOP/s (2*M*N*K per step, all ranks) over the device-timed
+region; ``roofline`` divides the dominant kernel's algorithmic FLOPs (or bytes, for the
+memory-bound skinny shape) by its mean CUDA-event duration; ``e2e`` repeats the metric
+through host buffers (pinned host -> device copies of A and B, the GEMM, and the copy of
+C back, every step); ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample.
+
+``--impl reference`` times the CPU oracle itself (the only reference this method has)
+on the same workload, one bounded sample per step.
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the product is
+single-GPU; there is no data-path collective), and the timing is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense tensor peak (1 GPU) vs CPU oracle"
+DATASHEET_BF16_TFLOPS = 2250.0  # dense bf16, NVIDIA GB300 (nominal)
+TF32_OVER_BF16 = 1100.0 / 2250.0  # nominal dense tf32 / bf16 ratio
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_bf16_8192.md")
+TC_SOURCE = os.path.join(ROOT, "dense_tiled_gemm_05_gb300", "csrc", "tc_kernel.cu")
+
+
+def workload(name):
+    """(problem, description, bound) for a named workload."""
+    if name == "bf16_8192":
+        return (W.bf16_square(8192, seed=5),
+                "bf16 GEMM M=N=K=8192, A row-major, B column-major, N(0,1)/sqrt(K), "
+                "fp32 accumulate, bf16 out", "tensor")
+    if name == "bf16_4096":
+        return (W.bf16_square(4096), "bf16 GEMM M=N=K=4096, A row-major, B column-major, "
+                "N(0,1)/sqrt(K), fp32 accumulate, bf16 out", "tensor")
+    if name == "tf32_4096":
+        return (W.fp32_square(4096, "tf32"), "fp32 GEMM M=N=K=4096 row-major, U[-1,1], tf32 "
+                "mode, fp32 out", "tensor")
+    if name == "exact_4096":
+        return (W.fp32_square(4096, "exact"), "fp32 GEMM M=N=K=4096 row-major, U[-1,1], "
+                "exact-fp32 mode, fp32 out", "alu")
+    if name == "bf16_skinny":
+        return (W.bf16_skinny(), "bf16 GEMM M=16384 N=128 K=8192, A row-major, B column-major, "
+                "N(0,1)/sqrt(K), fp32 accumulate, bf16 out (memory-bound)", "hbm")
+    raise SystemExit("unknown workload %s" % name)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK, "fallback"
+
+
+def algorithmic_bytes(p):
+    es = p.A.element_size()
+    return p.M * p.K * es + p.K * p.N * es + p.M * p.N * W.TORCH_DTYPES[p.out_dtype].itemsize
+
+
+def profile_traffic():
+    """dram bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not s:
+        return None
+    cur = hashlib.sha256(open(TC_SOURCE, "rb").read()).hexdigest()
+    return float(m.group(1)) if s.group(1) == cur else None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.device)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                self.samples.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                                     "hw_slowdown": f[5] == "Active",
+                                     "hw_thermal_slowdown": f[6] == "Active",
+                                     "sw_thermal_slowdown": f[7] == "Active",
+                                     "sw_power_cap": f[8] == "Active"})
+            except ValueError:
+                continue
+        return False
+
+    def summary(self):
+        s = getattr(self, "samples", [])
+        if not s:
+            return None
+        loaded = [x for x in s if x["power"] > 300.0] or s
+        reasons = sorted({k for x in loaded for k in ("hw_slowdown", "hw_thermal_slowdown",
+                                                      "sw_thermal_slowdown", "sw_power_cap")
+                          if x[k]})
+        return {"sm_mhz": statistics.median(x["sm"] for x in loaded),
+                "sm_max_mhz": max(x["max"] for x in s), "reasons": reasons,
+                "samples": len(s), "samples_under_load": len(loaded),
+                "power_w_max": max(x["power"] for x in s)}
+
+
+def cpu_baseline(p, target_s=10.0):
+    """The oracle as it stands on a bounded sample of output rows (all columns)."""
+    import oracle
+    a, al, lda = W.storage_numpy(p.A)
+    b, bl, ldb = W.storage_numpy(p.B)
+    kw = dict(lda=lda, ldb=ldb, a_dtype=p.in_dtype, b_dtype=W.dtype_name(p.B.dtype),
+              a_layout=al, b_layout=bl)
+    rows = 8
+    t0 = time.perf_counter()
+    oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=np.arange(rows), **kw)
+    t_probe = time.perf_counter() - t0
+    rows = int(max(8, min(p.M, rows * target_s / max(t_probe, 1e-3))))
+    sel = np.linspace(0, p.M - 1, rows).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=sel, **kw)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * p.N * p.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d output rows (all %d columns, K=%d) in fp64, %.1f s, OpenMP"
+                      % (rows, p.M, p.N, p.K, dt)}
+
+
+def run_reference(args, p, desc):
+    """--impl reference: the CPU oracle timed per step on a bounded block of the output."""
+    import oracle
+    a, al, lda = W.storage_numpy(p.A)
+    b, bl, ldb = W.storage_numpy(p.B)
+    kw = dict(lda=lda, ldb=ldb, a_dtype=p.in_dtype, b_dtype=W.dtype_name(p.B.dtype),
+              a_layout=al, b_layout=bl)
+    # One step computes an r x c block of C over the full K: rows spread over M, and the
+    # first c columns of B (same storage and leading dimension, so only they are decoded).
+    budget = 120.0 / max(1, args.steps + args.warmup)
+
+    def block(r, c, i0):
+        rows = (np.arange(r) * 7919 + i0) % p.M
+        return oracle.gemm_f64(a, b, p.M, c, p.K, rows=rows, **kw)
+
+    r = c = 32
+    t0 = time.perf_counter()
+    block(r, c, 0)
+    t1 = time.perf_counter() - t0
+    scale = max(1.0, budget / max(t1, 1e-4))
+    r = int(max(1, min(p.M, r * scale ** 0.5)))
+    c = int(max(1, min(p.N, c * scale ** 0.5)))
+    for i in range(args.warmup):
+        block(r, c, i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        block(r, c, 1000 + i)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * r * c * p.K * args.steps
+    value = flops / dt / 1e12
+    cores = oracle.num_threads()
+    sample = "per step a %d x %d block of C over K=%d, fp64 oracle, OpenMP" % (r, c, p.K)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "M": p.M, "N": p.N, "K": p.K},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bf16_8192")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rotate", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    p, desc, bound = workload(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, p, desc)), flush=True)
+        return
+
+    import dense_tiled_gemm_05_gb300 as g
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    h = g.Gemm(local_rank)
+    stream = torch.cuda.current_stream(dev)
+
+    # Inputs resident in HBM: `rotate` buffer sets so consecutive steps do not hit in L2.
+    a0 = torch.as_strided(torch.empty(p.A.numel(), dtype=p.A.dtype, device=dev), p.A.shape,
+                          p.A.stride())
+    b0 = torch.as_strided(torch.empty(p.B.numel(), dtype=p.B.dtype, device=dev), p.B.shape,
+                          p.B.stride())
+    a0.copy_(p.A)
+    b0.copy_(p.B)
+    sets = [(a0, b0)]
+    for _ in range(1, max(1, args.rotate)):
+        a1 = torch.empty_strided(a0.shape, a0.stride(), dtype=a0.dtype, device=dev)
+        b1 = torch.empty_strided(b0.shape, b0.stride(), dtype=b0.dtype, device=dev)
+        a1.copy_(a0)
+        b1.copy_(b0)
+        sets.append((a1, b1))
+    out_dt = W.TORCH_DTYPES[p.out_dtype]
+    outs = [torch.empty((p.M, p.N), dtype=out_dt, device=dev) for _ in sets]
+
+    def step(i):
+        a, b = sets[i % len(sets)]
+        h.matmul(a, b, out=outs[i % len(sets)], precision=p.precision, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if h.status() != 0:
+        raise SystemExit("device status error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = h.launch_count()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t_start.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    launches = h.launch_count() - launches0
+    if h.status() != 0:
+        raise SystemExit("device status error in the timed region")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    flops = 2.0 * p.M * p.N * p.K
+    value = world * flops * args.steps / (elapsed_ms / 1e3) / 1e12
+    peaks, peak_src = measured_peaks()
+    if bound == "hbm":
+        achieved = algorithmic_bytes(p) / (kernel_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": "%s hbm_gbs (copy)" % peak_src}
+    elif bound == "alu":
+        props = torch.cuda.get_device_properties(dev)
+        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+        achieved = flops / (kernel_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": "%d SMs x 128 fp32 FMA/clk x 2 x %.0f MHz"
+                               % (props.multi_processor_count, sm_mhz)}
+    else:
+        achieved = flops / (kernel_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        src = "%s bf16_tflops (cuBLAS burst)" % peak_src
+        if p.in_dtype == "f32":
+            peak *= TF32_OVER_BF16
+            src += " x nominal tf32/bf16 ratio %.3f" % TF32_OVER_BF16
+        traffic = profile_traffic() if args.workload == "bf16_8192" else None
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": src,
+                "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] *
+                                                 (TF32_OVER_BF16 if p.in_dtype == "f32" else 1))}
+
+    # End to end through host buffers: pinned A, B in, C out, every step.
+    e2e = None
+    if not args.no_e2e:
+        ha = torch.empty_strided(p.A.shape, p.A.stride(), dtype=p.A.dtype, pin_memory=True)
+        hb = torch.empty_strided(p.B.shape, p.B.stride(), dtype=p.B.dtype, pin_memory=True)
+        ha.copy_(p.A)
+        hb.copy_(p.B)
+        hc = torch.empty((p.M, p.N), dtype=out_dt, pin_memory=True)
+        work = {"a": sets[0][0], "b": sets[0][1], "c": outs[0]}
+        for _ in range(3):
+            g.matmul_host(ha, hb, out=hc, precision=p.precision, device=local_rank, work=work)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            g.matmul_host(ha, hb, out=hc, precision=p.precision, device=local_rank, work=work)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        if h.status() != 0:
+            raise SystemExit("device status error in the e2e region")
+        e2e = {"value": world * flops * args.e2e_steps / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": ha.numel() * ha.element_size() + hb.numel() * hb.element_size(),
+               "d2h_bytes_per_step": hc.numel() * hc.element_size(),
+               "ms_per_step": e_ms / args.e2e_steps}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "f16": "f16", "f32": "tf32" if p.precision == "tf32" else "f32"}[
+            p.in_dtype],
+        "data": "synthetic",
+        "config": {"workload": desc, "M": p.M, "N": p.N, "K": p.K,
+                   "l2": "inputs larger than L2, rotated over %d buffer sets" % len(sets),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_datasheet_bf16_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
+        "roofline": roof,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    h.close()
+
+
+if __name__ == "__main__":
+    main()

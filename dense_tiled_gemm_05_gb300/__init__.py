@@ -1,0 +1,292 @@
+"""Python binding of the GB300 blocked-GEMM library (``include/gemm.h``).
+
+The binding only marshals arguments: it reads shapes, strides, data pointers
+and the current CUDA stream from torch tensors and calls the C ABI through
+ctypes. Every step of the product runs in the library's own CUDA kernels; if
+the compiled library is missing, importing the binding's entry points raises
+instead of falling back to anything else.
+
+    import dense_tiled_gemm_05_gb300 as g
+    c = g.matmul(a, b)                       # a: M x K, b: K x N, CUDA tensors
+    c = g.matmul(a32, b32, precision="tf32") # fp32 inputs on the tf32 tensor cores
+
+Layouts follow the tensors' strides: a row-major view has stride (ld, 1), a
+column-major view stride (1, ld) (e.g. ``b_storage.t()`` for a B stored as
+[N, K]). The output is row-major.
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libgemm_gb300.so")
+
+# enums of include/gemm.h
+F32, F16, BF16 = 0, 1, 2
+PREC = {"default": 0, "tf32": 1, "exact": 2}
+ROW, COL = 0, 1
+STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
+          3: "GEMM_ERR_ALIGNMENT", 4: "GEMM_ERR_NO_MEMORY", 5: "GEMM_ERR_CUDA",
+          6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_DEVICE"}
+OPTIONS = {"wait_timeout_us": 0, "force_path": 1, "group_m": 2, "max_ctas": 3,
+           "fault_stall_producer": 4, "force_staging": 5}
+PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma"}
+_DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+_DT_NAMES = {"f32": F32, "f16": F16, "bf16": BF16}
+_TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
+
+# Every symbol include/gemm.h declares.
+EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
+           "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
+           "gemm_version")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+        super().__init__("%s%s (%s)" % (what + ": " if what else "", self.status, _strerror(code)))
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("tile_k", ctypes.c_int32), ("grid_m", ctypes.c_int64), ("grid_n", ctypes.c_int64),
+                ("k_iters", ctypes.c_int64), ("stages", ctypes.c_int32), ("stage_a", ctypes.c_int32),
+                ("stage_b", ctypes.c_int32), ("a_mn_major", ctypes.c_int32),
+                ("b_mn_major", ctypes.c_int32), ("tma_store", ctypes.c_int32),
+                ("ctas", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["path"] = PATHS.get(d["path"], d["path"])
+        return d
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib():
+    """The loaded C library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        with _lib_lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        "libgemm_gb300.so is not built; run "
+                        "`python -c 'import __graft_entry__ as g; g.build()'` "
+                        "(or python dense_tiled_gemm_05_gb300/build.py)")
+                L = ctypes.CDLL(LIB_PATH)
+                i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+                run_args = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32]
+                L.gemm_create.argtypes = [ctypes.POINTER(vp), i32]
+                L.gemm_create.restype = i32
+                L.gemm_destroy.argtypes = [vp]
+                L.gemm_destroy.restype = None
+                L.gemm_run.argtypes = run_args
+                L.gemm_run.restype = i32
+                L.gemm_run_ex.argtypes = run_args + [i32, i32, vp]
+                L.gemm_run_ex.restype = i32
+                L.gemm_get_status.argtypes = [vp, vp]
+                L.gemm_get_status.restype = i32
+                L.gemm_strerror.argtypes = [i32]
+                L.gemm_strerror.restype = ctypes.c_char_p
+                L.gemm_set_option.argtypes = [vp, i32, i64]
+                L.gemm_set_option.restype = i32
+                L.gemm_get_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+                L.gemm_get_launch_count.restype = i32
+                L.gemm_plan.argtypes = run_args + [i32, i32, ctypes.c_int32,
+                                                   ctypes.POINTER(PlanInfo)]
+                L.gemm_plan.restype = i32
+                L.gemm_version.argtypes = []
+                L.gemm_version.restype = ctypes.c_char_p
+                _lib = L
+    return _lib
+
+
+def _strerror(code):
+    try:
+        return lib().gemm_strerror(code).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(code, what=""):
+    if code != 0:
+        raise GemmError(code, what)
+
+
+def operand_layout(x):
+    """(layout, ld) of a 2-D view: ROW for stride (ld, 1), COL for stride (1, ld)."""
+    if x.dim() != 2:
+        raise ValueError("operands must be 2-D")
+    r, c = x.shape
+    s0, s1 = x.stride()
+    if s1 == 1 and (s0 >= max(c, 1) or r <= 1):
+        return ROW, max(s0, c, 1)
+    if s0 == 1 and (s1 >= max(r, 1) or c <= 1):
+        return COL, max(s1, r, 1)
+    raise ValueError("operand must be row- or column-major, got stride %s" % (x.stride(),))
+
+
+def _dtype_code(d):
+    if isinstance(d, str):
+        return _DT_NAMES[d]
+    if d in _DT:
+        return _DT[d]
+    raise TypeError("unsupported dtype %s" % d)
+
+
+class Gemm:
+    """A library handle bound to one CUDA device."""
+
+    def __init__(self, device=None):
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = int(device)
+        h = ctypes.c_void_p()
+        _check(lib().gemm_create(ctypes.byref(h), self.device), "gemm_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().gemm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    def set_option(self, name, value):
+        _check(lib().gemm_set_option(self._h, OPTIONS[name], int(value)), "gemm_set_option")
+
+    def launch_count(self):
+        n = ctypes.c_uint64()
+        _check(lib().gemm_get_launch_count(self._h, ctypes.byref(n)))
+        return n.value
+
+    def status(self, stream=None):
+        """Synchronise the stream and return the device status code (0 = OK), cleared."""
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        return lib().gemm_get_status(self._h, ctypes.c_void_p(s.cuda_stream))
+
+    def run_raw(self, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision=0,
+                a_layout=ROW, b_layout=COL, stream=0):
+        """Direct C-ABI call with integer pointers; returns the status code."""
+        return lib().gemm_run_ex(self._h, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype,
+                                 precision, a_layout, b_layout, ctypes.c_void_p(stream))
+
+    def matmul(self, a, b, out=None, out_dtype=None, precision="default", stream=None):
+        """C = a @ b on the GPU; a is M x K, b is K x N (row- or column-major views)."""
+        if a.dtype != b.dtype:
+            raise TypeError("a and b must share a dtype")
+        if not (a.is_cuda and b.is_cuda):
+            raise ValueError("operands must be CUDA tensors (see matmul_host for host buffers)")
+        M, K = a.shape
+        K2, N = b.shape
+        if K != K2:
+            raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+        in_dt = _dtype_code(a.dtype)
+        if out is None:
+            od = _TORCH_OF[_dtype_code(out_dtype)] if out_dtype is not None else a.dtype
+            out = torch.empty((M, N), dtype=od, device=a.device)
+        if out.dim() != 2 or out.shape != (M, N) or (N > 1 and out.stride(1) != 1):
+            raise ValueError("out must be a row-major M x N tensor")
+        al, lda = operand_layout(a)
+        bl, ldb = operand_layout(b)
+        ldc = max(out.stride(0), N, 1)
+        s = torch.cuda.current_stream(a.device) if stream is None else stream
+        code = lib().gemm_run_ex(self._h, M, N, K, ctypes.c_void_p(a.data_ptr()), lda,
+                                 ctypes.c_void_p(b.data_ptr()), ldb,
+                                 ctypes.c_void_p(out.data_ptr()), ldc, in_dt,
+                                 _dtype_code(out.dtype), PREC[precision], al, bl,
+                                 ctypes.c_void_p(s.cuda_stream))
+        _check(code, "gemm_run_ex")
+        return out
+
+    def plan(self, a, b, out=None, out_dtype=None, precision="default", sm_count=None):
+        """The planner's decision for these operands (host-only, nothing launched)."""
+        return plan(a, b, out=out, out_dtype=out_dtype, precision=precision,
+                    sm_count=sm_count, handle=self)
+
+
+def plan(a, b, out=None, out_dtype=None, precision="default", sm_count=148, handle=None,
+         a_ptr=None, b_ptr=None, c_ptr=None, ldc=None):
+    """Host-only planner query (works without a GPU); returns a dict.
+
+    Pointers default to the tensors' data pointers; pass integers to ask about
+    alignments the tensors do not have.
+    """
+    M, K = a.shape
+    N = b.shape[1]
+    al, lda = operand_layout(a)
+    bl, ldb = operand_layout(b)
+    od = _dtype_code(out_dtype) if out_dtype is not None else (
+        _dtype_code(out.dtype) if out is not None else _dtype_code(a.dtype))
+    if ldc is None:
+        ldc = max(out.stride(0), N, 1) if out is not None else max(N, 1)
+    if c_ptr is None:
+        c_ptr = out.data_ptr() if out is not None else 1 << 20
+    info = PlanInfo()
+    code = lib().gemm_plan(handle.handle if handle is not None else None, M, N, K,
+                           ctypes.c_void_p(a.data_ptr() if a_ptr is None else a_ptr), lda,
+                           ctypes.c_void_p(b.data_ptr() if b_ptr is None else b_ptr), ldb,
+                           ctypes.c_void_p(c_ptr), ldc, _dtype_code(a.dtype), od,
+                           PREC[precision], al, bl, int(sm_count or 148), ctypes.byref(info))
+    _check(code, "gemm_plan")
+    return info.as_dict()
+
+
+_handles = {}
+
+
+def handle(device=None):
+    """The per-device default handle (created on first use)."""
+    dev = torch.cuda.current_device() if device is None else int(device)
+    h = _handles.get(dev)
+    if h is None:
+        h = _handles[dev] = Gemm(dev)
+    return h
+
+
+def matmul(a, b, out=None, out_dtype=None, precision="default"):
+    """C = a @ b with the default handle of a's device; see :meth:`Gemm.matmul`."""
+    return handle(a.device.index).matmul(a, b, out=out, out_dtype=out_dtype, precision=precision)
+
+
+def matmul_host(a, b, out=None, out_dtype=None, precision="default", device=None, work=None):
+    """End-to-end product of HOST tensors: copy a and b to the GPU, multiply, copy C back.
+
+    ``work`` may hold preallocated device tensors {"a", "b", "c"} to reuse.
+    Host tensors should be pinned for asynchronous copies.
+    """
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    if work is None:
+        work = {}
+    da = work.get("a")
+    if da is None:
+        da = torch.empty_strided(a.shape, a.stride(), dtype=a.dtype, device=dev)
+    db = work.get("b")
+    if db is None:
+        db = torch.empty_strided(b.shape, b.stride(), dtype=b.dtype, device=dev)
+    da.copy_(a, non_blocking=True)
+    db.copy_(b, non_blocking=True)
+    dc = handle(dev.index).matmul(da, db, out=work.get("c"), out_dtype=out_dtype,
+                                  precision=precision)
+    if out is None:
+        out = torch.empty(dc.shape, dtype=dc.dtype, pin_memory=True)
+    out.copy_(dc, non_blocking=True)
+    return out
+
+
+def version():
+    return lib().gemm_version().decode()

@@ -1,0 +1,191 @@
+// fma_kernel.cu -- exact-fp32 tile kernel, operand staging and zero fill.
+//
+// The FMA kernel is the blocked matrix multiply of "Chapter 13: The Blocked Matmul
+// Kernel", section 13.1, Worked Example 13.1.1, done with fp32 fused multiply-adds:
+// one CTA per BM x BN output tile on a 2D grid (ceil(N/BN), ceil(M/BM)), a K-loop of
+// ceil(K/BK) chunks, an fp32 accumulator initialised once before the loop, loads masked
+// by rows < M, k < K and cols < N with zeros outside (section 13.2's three masks), and a
+// store masked by rows < M and cols < N. It serves the exact-fp32 mode ("Triton matmul",
+// the "Precision" section: tf32 is not exact) and, with 4 x 4 x 4 tiles, the pages' own
+// 8 x 8 x 8 example (grid 2 x 2, two K-iterations per tile).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float load_as_float(const void *base, int64_t idx) {
+  return static_cast<float>(reinterpret_cast<const T *>(base)[idx]);
+}
+template <>
+__device__ __forceinline__ float load_as_float<__half>(const void *base, int64_t idx) {
+  return __half2float(reinterpret_cast<const __half *>(base)[idx]);
+}
+template <>
+__device__ __forceinline__ float load_as_float<__nv_bfloat16>(const void *base, int64_t idx) {
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+}
+
+__device__ __forceinline__ void store_out(void *C, int64_t idx, int out_dtype, float v) {
+  if (out_dtype == GEMM_F32)
+    reinterpret_cast<float *>(C)[idx] = v;
+  else if (out_dtype == GEMM_BF16)
+    reinterpret_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<__half *>(C)[idx] = __float2half_rn(v);
+}
+
+// Row (or column) of the tile owned by thread coordinate t for its i-th register. With
+// 8 registers the thread's rows are split into two groups of 4, half a tile apart, so
+// that the shared-memory reads of a warp fall into distinct banks.
+template <int T, int BLK>
+__device__ __forceinline__ int owned(int t, int i) {
+  if (T >= 8) return i < T / 2 ? t * (T / 2) + i : BLK / 2 + t * (T / 2) + (i - T / 2);
+  return t * T + i;
+}
+
+template <int BM, int BN, int BK, int TM, int TN, typename InT>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+    fma_gemm_kernel(const FmaParams p) {
+  constexpr int TX = BN / TN, TY = BM / TM, NT = TX * TY;
+  __shared__ float As[BK][BM];
+  __shared__ float Bs[BK][BN];
+  const int tid = threadIdx.x;
+  const int tx = tid % TX, ty = tid / TX;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
+
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;  // initialised once, before the K-loop
+
+  for (int64_t k0 = 0; k0 < p.K; k0 += BK) {
+    // A tile: rows m0.., k-columns k0..; walk the storage's contiguous axis fastest.
+    for (int e = tid; e < BM * BK; e += NT) {
+      const int r = p.a_col ? e % BM : e / BK;
+      const int kk = p.a_col ? e / BM : e % BK;
+      const int64_t i = m0 + r, k = k0 + kk;
+      float v = 0.0f;
+      if (i < p.M && k < p.K) v = load_as_float<InT>(p.A, p.a_col ? k * p.lda + i : i * p.lda + k);
+      As[kk][r] = v;
+    }
+    for (int e = tid; e < BK * BN; e += NT) {
+      const int c = p.b_col ? e / BK : e % BN;
+      const int kk = p.b_col ? e % BK : e / BN;
+      const int64_t j = n0 + c, k = k0 + kk;
+      float v = 0.0f;
+      if (j < p.N && k < p.K) v = load_as_float<InT>(p.B, p.b_col ? j * p.ldb + k : k * p.ldb + j);
+      Bs[kk][c] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; ++i) a[i] = As[kk][owned<TM, BM>(ty, i)];
+#pragma unroll
+      for (int j = 0; j < TN; ++j) b[j] = Bs[kk][owned<TN, BN>(tx, j)];
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int64_t row = m0 + owned<TM, BM>(ty, i);
+    if (row >= p.M) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int64_t col = n0 + owned<TN, BN>(tx, j);
+      if (col < p.N) store_out(p.C, row * p.ldc + col, p.out_dtype, acc[i][j]);
+    }
+  }
+}
+
+template <int BM, int BN, int BK, int TM, int TN>
+cudaError_t fma_launch_tile(const FmaParams &p, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((p.N + BN - 1) / BN),
+                  static_cast<unsigned>((p.M + BM - 1) / BM));
+  const dim3 block((BM / TM) * (BN / TN));
+  if (p.in_dtype == GEMM_F32)
+    fma_gemm_kernel<BM, BN, BK, TM, TN, float><<<grid, block, 0, s>>>(p);
+  else if (p.in_dtype == GEMM_F16)
+    fma_gemm_kernel<BM, BN, BK, TM, TN, __half><<<grid, block, 0, s>>>(p);
+  else
+    fma_gemm_kernel<BM, BN, BK, TM, TN, __nv_bfloat16><<<grid, block, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void repack_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
+                              int64_t ld_dst, int64_t outer, int64_t inner) {
+  for (int64_t o = blockIdx.y; o < outer; o += gridDim.y)
+    for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < inner;
+         x += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      dst[o * ld_dst + x] = src[o * ld_src + x];
+}
+
+template <typename T>
+__global__ void zero_fill_kernel(T *C, int64_t ldc, int64_t M, int64_t N) {
+  for (int64_t i = blockIdx.y; i < M; i += gridDim.y)
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < N;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      C[i * ldc + j] = T(0);
+}
+
+dim3 grid_2d(int64_t outer, int64_t inner, int threads) {
+  const int64_t gx = (inner + threads - 1) / threads;
+  return dim3(static_cast<unsigned>(gx < 64 ? (gx < 1 ? 1 : gx) : 64),
+              static_cast<unsigned>(outer < 65535 ? (outer < 1 ? 1 : outer) : 65535));
+}
+
+}  // namespace
+
+void fma_tile_shape(int tile, int *bm, int *bn, int *bk) {
+  if (tile == 4) {
+    *bm = 4, *bn = 4, *bk = 4;
+  } else {
+    *bm = 128, *bn = 128, *bk = 8;
+  }
+}
+
+cudaError_t fma_launch(const FmaParams &p, int tile, cudaStream_t s) {
+  if (tile == 4) return fma_launch_tile<4, 4, 4, 1, 1>(p, s);
+  return fma_launch_tile<128, 128, 8, 8, 8>(p, s);
+}
+
+cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                          int64_t outer, int64_t inner, int esize, cudaStream_t s) {
+  const int threads = 256;
+  const dim3 grid = grid_2d(outer, inner, threads);
+  if (esize == 2)
+    repack_kernel<uint16_t><<<grid, threads, 0, s>>>(static_cast<const uint16_t *>(src), ld_src,
+                                                     static_cast<uint16_t *>(dst), ld_dst, outer,
+                                                     inner);
+  else
+    repack_kernel<uint32_t><<<grid, threads, 0, s>>>(static_cast<const uint32_t *>(src), ld_src,
+                                                     static_cast<uint32_t *>(dst), ld_dst, outer,
+                                                     inner);
+  return cudaGetLastError();
+}
+
+cudaError_t zero_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, int out_dtype,
+                             cudaStream_t s) {
+  const int threads = 256;
+  const dim3 grid = grid_2d(M, N, threads);
+  if (out_dtype == GEMM_F32)
+    zero_fill_kernel<uint32_t><<<grid, threads, 0, s>>>(static_cast<uint32_t *>(C), ldc, M, N);
+  else
+    zero_fill_kernel<uint16_t><<<grid, threads, 0, s>>>(static_cast<uint16_t *>(C), ldc, M, N);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,579 @@
+// gemm_api.cu -- host runtime behind include/gemm.h: handle, argument checks, planner,
+// operand staging, tensor-map encoding and kernel launch.
+//
+// The host wrapper of "Chapter 13: The Blocked Matmul Kernel" (section 13.4,
+// 01_tiled_matmul.py) reads M, K from A and N from B, checks that the inner dimensions
+// agree, lets the caller own C, and launches a (cdiv(M, BLOCK_M), cdiv(N, BLOCK_N)) grid
+// with cdiv(K, BLOCK_K) K-iterations per tile. Here the caller states M, N, K and the
+// leading dimensions explicitly (the pages pass all six strides), and the planner maps
+// the same tile grid onto a persistent schedule of one CTA per SM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.h"
+#include "internal.h"
+
+using namespace gemm_gb300;
+
+struct gemm_handle_s {
+  int device = 0;
+  int sm_count = 0;
+  int *status = nullptr;  // device status word
+  void *workspace = nullptr;
+  size_t workspace_bytes = 0;
+  uint64_t launches = 0;
+  // options
+  uint64_t timeout_us = 2000000;
+  int force_path = 0;
+  int group_m = 8;
+  int max_ctas = 0;
+  int stall_producer = 0;
+  int force_staging = 0;
+};
+
+namespace {
+
+const char *kVersion = "0.1.0";
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char *e = std::getenv("GEMM_LOG");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+gemm_status_t cuda_fail(cudaError_t e, const char *what) {
+  if (log_enabled()) std::fprintf(stderr, "[gemm] %s: %s\n", what, cudaGetErrorString(e));
+  return GEMM_ERR_CUDA;
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the library
+// needs no link-time dependency on libcuda.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int esize_of(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+
+bool valid_dtype(int d) { return d == GEMM_F32 || d == GEMM_F16 || d == GEMM_BF16; }
+bool valid_layout(int l) { return l == GEMM_ROW_MAJOR || l == GEMM_COL_MAJOR; }
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Byte span [lo, hi) touched by a rows x cols operand with the given layout.
+void span_of(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout, int es,
+             uintptr_t *lo, uintptr_t *hi) {
+  const int64_t outer = layout == GEMM_ROW_MAJOR ? rows : cols;
+  const int64_t inner = layout == GEMM_ROW_MAJOR ? cols : rows;
+  *lo = reinterpret_cast<uintptr_t>(p);
+  *hi = *lo + static_cast<uintptr_t>(((outer - 1) * ld + inner) * es);
+}
+
+struct Problem {
+  int64_t M, N, K;
+  const void *A;
+  int64_t lda;
+  const void *B;
+  int64_t ldb;
+  void *C;
+  int64_t ldc;
+  int in_dtype, out_dtype, precision, a_layout, b_layout;
+};
+
+struct Options {
+  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0;
+};
+
+// An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
+// elements with leading dimension ld (in elements), possibly staged into the workspace.
+struct OperandPlan {
+  const void *ptr;
+  int64_t ld, outer, inner;
+  bool mn_major;
+  bool staged;
+  int64_t staged_ld;
+  size_t ws_offset, ws_bytes;
+};
+
+struct Plan {
+  gemm_plan_info_t info;
+  TcVariant variant;
+  OperandPlan a, b;
+  int fma_tile;
+};
+
+gemm_status_t check_args(const Problem &P) {
+  if (P.M < 0 || P.N < 0 || P.K < 0) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(P.in_dtype) || !valid_dtype(P.out_dtype)) return GEMM_ERR_INVALID_ARG;
+  if (!valid_layout(P.a_layout) || !valid_layout(P.b_layout)) return GEMM_ERR_INVALID_ARG;
+  if (P.precision < GEMM_PREC_DEFAULT || P.precision > GEMM_PREC_EXACT_FP32)
+    return GEMM_ERR_INVALID_ARG;
+  const bool a_used = P.M > 0 && P.K > 0 && P.N > 0;
+  const bool b_used = P.K > 0 && P.N > 0 && P.M > 0;
+  const bool c_used = P.M > 0 && P.N > 0;
+  if (c_used) {
+    if (!P.C || P.ldc < P.N) return GEMM_ERR_INVALID_ARG;
+  }
+  if (a_used) {
+    if (!P.A) return GEMM_ERR_INVALID_ARG;
+    if (P.lda < (P.a_layout == GEMM_ROW_MAJOR ? P.K : P.M)) return GEMM_ERR_INVALID_ARG;
+  }
+  if (b_used) {
+    if (!P.B) return GEMM_ERR_INVALID_ARG;
+    if (P.ldb < (P.b_layout == GEMM_ROW_MAJOR ? P.N : P.K)) return GEMM_ERR_INVALID_ARG;
+  }
+  if (P.in_dtype != GEMM_F32 && P.precision != GEMM_PREC_DEFAULT) return GEMM_ERR_UNSUPPORTED;
+  if (P.M > INT32_MAX || P.N > INT32_MAX || P.K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  const int es = esize_of(P.in_dtype), os = esize_of(P.out_dtype);
+  if ((a_used && reinterpret_cast<uintptr_t>(P.A) % es) ||
+      (b_used && reinterpret_cast<uintptr_t>(P.B) % es) ||
+      (c_used && reinterpret_cast<uintptr_t>(P.C) % os))
+    return GEMM_ERR_ALIGNMENT;
+  if (c_used) {
+    uintptr_t clo, chi;
+    span_of(P.C, P.M, P.N, P.ldc, GEMM_ROW_MAJOR, os, &clo, &chi);
+    if (a_used) {
+      uintptr_t lo, hi;
+      span_of(P.A, P.M, P.K, P.lda, P.a_layout, es, &lo, &hi);
+      if (clo < hi && lo < chi) return GEMM_ERR_INVALID_ARG;
+    }
+    if (b_used) {
+      uintptr_t lo, hi;
+      span_of(P.B, P.K, P.N, P.ldb, P.b_layout, es, &lo, &hi);
+      if (clo < hi && lo < chi) return GEMM_ERR_INVALID_ARG;
+    }
+  }
+  return GEMM_OK;
+}
+
+// TMA can read an operand in place when its base is 16-byte aligned and its leading
+// dimension is a multiple of 16 bytes (a single line needs no stride).
+bool tma_legal(const void *p, int64_t ld, int64_t outer, int es) {
+  if (reinterpret_cast<uintptr_t>(p) % 16) return false;
+  return outer <= 1 || (ld * es) % 16 == 0;
+}
+
+OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout,
+                         bool k_is_rows_dim, int es, bool force_stage, size_t *ws_cursor) {
+  OperandPlan o{};
+  o.ptr = p;
+  o.ld = ld;
+  o.outer = layout == GEMM_ROW_MAJOR ? rows : cols;
+  o.inner = layout == GEMM_ROW_MAJOR ? cols : rows;
+  // The operand is K-major when K is its contiguous axis.
+  const bool k_inner = k_is_rows_dim ? layout == GEMM_COL_MAJOR : layout == GEMM_ROW_MAJOR;
+  o.mn_major = !k_inner;
+  o.staged = force_stage || !tma_legal(p, ld, o.outer, es);
+  if (o.staged) {
+    o.staged_ld = round_up(o.inner, 16 / es);
+    o.ws_offset = *ws_cursor;
+    o.ws_bytes = static_cast<size_t>(o.staged_ld * o.outer * es);
+    *ws_cursor = static_cast<size_t>(round_up(static_cast<int64_t>(*ws_cursor + o.ws_bytes), 256));
+  }
+  return o;
+}
+
+gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan *out) {
+  gemm_status_t st = check_args(P);
+  if (st != GEMM_OK) return st;
+  Plan pl{};
+  gemm_plan_info_t &I = pl.info;
+  if (P.M == 0 || P.N == 0) {
+    I.path = GEMM_PATH_NONE;
+    *out = pl;
+    return GEMM_OK;
+  }
+  if (P.K == 0) {
+    I.path = GEMM_PATH_ZERO_FILL;
+    I.ctas = 1;
+    *out = pl;
+    return GEMM_OK;
+  }
+  const bool exact = P.in_dtype == GEMM_F32 && P.precision != GEMM_PREC_TF32;
+  bool use_fma = exact;
+  if (opt.force_path == 2) use_fma = true;
+  if (opt.force_path == 1) {
+    if (exact) return GEMM_ERR_UNSUPPORTED;  // the tensor cores have no exact-fp32 mode
+    use_fma = false;
+  }
+  if (use_fma) {
+    pl.fma_tile = (P.M * P.N <= 256) ? 4 : 128;
+    int bm, bn, bk;
+    fma_tile_shape(pl.fma_tile, &bm, &bn, &bk);
+    I.path = GEMM_PATH_FMA;
+    I.tile_m = bm, I.tile_n = bn, I.tile_k = bk;
+    I.grid_m = (P.M + bm - 1) / bm;
+    I.grid_n = (P.N + bn - 1) / bn;
+    I.k_iters = (P.K + bk - 1) / bk;
+    if (I.grid_m > 65535 || I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    I.ctas = I.grid_m * I.grid_n;
+    *out = pl;
+    return GEMM_OK;
+  }
+  const int es = esize_of(P.in_dtype);
+  const int os = esize_of(P.out_dtype);
+  size_t cursor = 0;
+  pl.a = plan_operand(P.A, P.M, P.K, P.lda, P.a_layout, false, es, opt.force_staging != 0, &cursor);
+  pl.b = plan_operand(P.B, P.K, P.N, P.ldb, P.b_layout, true, es, opt.force_staging != 0, &cursor);
+  pl.variant.esize = es;
+  pl.variant.a_mn = pl.a.mn_major;
+  pl.variant.b_mn = pl.b.mn_major;
+  pl.variant.block_n = 256;
+  I.path = GEMM_PATH_TCGEN05;
+  I.tile_m = kTcBlockM;
+  I.tile_n = pl.variant.block_n;
+  I.tile_k = 128 / es;
+  I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
+  I.grid_n = (P.N + I.tile_n - 1) / I.tile_n;
+  I.k_iters = (P.K + I.tile_k - 1) / I.tile_k;
+  if (I.grid_m * I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  I.stages = tc_stages(pl.variant);
+  I.stage_a = pl.a.staged, I.stage_b = pl.b.staged;
+  I.a_mn_major = pl.a.mn_major, I.b_mn_major = pl.b.mn_major;
+  I.tma_store = reinterpret_cast<uintptr_t>(P.C) % 16 == 0 && (P.ldc * os) % 16 == 0;
+  const int64_t tiles = I.grid_m * I.grid_n;
+  int64_t ctas = sm_count > 0 ? sm_count : 1;
+  if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
+  I.ctas = tiles < ctas ? tiles : ctas;
+  I.workspace_bytes = static_cast<int64_t>(cursor);
+  *out = pl;
+  return GEMM_OK;
+}
+
+CUtensorMapDataType tmap_dtype(int dt) {
+  switch (dt) {
+    case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  }
+}
+
+// 2D tensor map: dims {inner, outer}, row pitch ld elements, box {box_inner, box_outer},
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_2d(CUtensorMap *m, int dtype, const void *base, int64_t inner, int64_t outer,
+               int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int es = esize_of(dtype);
+  int64_t pitch = ld * es;
+  if (outer <= 1) pitch = round_up(inner * es, 16);  // a single line: any legal pitch
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, tmap_dtype(dtype), 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS && log_enabled())
+    std::fprintf(stderr, "[gemm] cuTensorMapEncodeTiled failed (%d)\n", static_cast<int>(r));
+  return r == CUDA_SUCCESS;
+}
+
+uint32_t make_idesc(int in_dtype, bool a_mn, bool b_mn, int n, int m) {
+  const uint32_t fmt = in_dtype == GEMM_F16 ? 0u : in_dtype == GEMM_BF16 ? 1u : 2u;
+  uint32_t d = 0;
+  d |= 1u << 4;                               // accumulator: f32
+  d |= fmt << 7;                              // A format
+  d |= fmt << 10;                             // B format
+  d |= (a_mn ? 1u : 0u) << 15;                // A major-ness (1 = MN-major)
+  d |= (b_mn ? 1u : 0u) << 16;                // B major-ness
+  d |= static_cast<uint32_t>(n >> 3) << 17;   // N / 8
+  d |= static_cast<uint32_t>(m >> 4) << 24;   // M / 16
+  return d;
+}
+
+gemm_status_t ensure_workspace(gemm_handle_t h, size_t bytes) {
+  if (bytes <= h->workspace_bytes) return GEMM_OK;
+  const char *fi = std::getenv("GEMM_FAULT_INJECT");
+  if (fi && std::strcmp(fi, "alloc") == 0) return GEMM_ERR_NO_MEMORY;
+  if (h->workspace) {
+    cudaFree(h->workspace);  // synchronises: no launched work still uses it
+    h->workspace = nullptr;
+    h->workspace_bytes = 0;
+  }
+  void *p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_MEMORY;
+  }
+  h->workspace = p;
+  h->workspace_bytes = bytes;
+  return GEMM_OK;
+}
+
+Options options_of(gemm_handle_t h) {
+  Options o;
+  if (h) {
+    o.force_path = h->force_path;
+    o.group_m = h->group_m;
+    o.max_ctas = h->max_ctas;
+    o.force_staging = h->force_staging;
+  }
+  return o;
+}
+
+gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s) {
+  const gemm_plan_info_t &I = pl.info;
+  cudaError_t e;
+  switch (I.path) {
+    case GEMM_PATH_NONE: return GEMM_OK;
+    case GEMM_PATH_ZERO_FILL:
+      e = zero_fill_launch(P.C, P.ldc, P.M, P.N, P.out_dtype, s);
+      if (e != cudaSuccess) return cuda_fail(e, "zero fill launch");
+      h->launches += 1;
+      return GEMM_OK;
+    case GEMM_PATH_FMA: {
+      FmaParams fp{P.M, P.N, P.K, P.A, P.lda, P.B, P.ldb, P.C, P.ldc, P.in_dtype, P.out_dtype,
+                   P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR};
+      e = fma_launch(fp, pl.fma_tile, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fma launch");
+      h->launches += 1;
+      return GEMM_OK;
+    }
+    default: break;
+  }
+  // Tensor-core path.
+  const int es = esize_of(P.in_dtype);
+  gemm_status_t st = ensure_workspace(h, static_cast<size_t>(I.workspace_bytes));
+  if (st != GEMM_OK) return st;
+  const void *a_ptr = pl.a.ptr;
+  int64_t a_ld = pl.a.ld;
+  const void *b_ptr = pl.b.ptr;
+  int64_t b_ld = pl.b.ld;
+  if (pl.a.staged) {
+    void *dst = static_cast<char *>(h->workspace) + pl.a.ws_offset;
+    e = repack_launch(pl.a.ptr, pl.a.ld, dst, pl.a.staged_ld, pl.a.outer, pl.a.inner, es, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stage A");
+    h->launches += 1;
+    a_ptr = dst, a_ld = pl.a.staged_ld;
+  }
+  if (pl.b.staged) {
+    void *dst = static_cast<char *>(h->workspace) + pl.b.ws_offset;
+    e = repack_launch(pl.b.ptr, pl.b.ld, dst, pl.b.staged_ld, pl.b.outer, pl.b.inner, es, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stage B");
+    h->launches += 1;
+    b_ptr = dst, b_ld = pl.b.staged_ld;
+  }
+  const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
+  CUtensorMap tmA, tmB, tmC;
+  std::memset(&tmC, 0, sizeof tmC);
+  // K-major operand: box = (one 128-byte row of K) x (tile rows); MN-major operand:
+  // box = (one 128-byte row of M or N) x (the stage's K rows).
+  const uint32_t a_box_outer = pl.a.mn_major ? row_elems : static_cast<uint32_t>(I.tile_m);
+  const uint32_t b_box_outer = pl.b.mn_major ? row_elems : static_cast<uint32_t>(I.tile_n);
+  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.inner, pl.a.outer, a_ld, row_elems, a_box_outer) ||
+      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.inner, pl.b.outer, b_ld, row_elems, b_box_outer))
+    return GEMM_ERR_CUDA;
+  if (I.tma_store) {
+    const uint32_t out_row = 128 / esize_of(P.out_dtype);
+    if (!encode_2d(&tmC, P.out_dtype, P.C, P.N, P.M, P.ldc, out_row, 32)) return GEMM_ERR_CUDA;
+  }
+  TcParams tp{};
+  tp.M = static_cast<int32_t>(P.M);
+  tp.N = static_cast<int32_t>(P.N);
+  tp.K = static_cast<int32_t>(P.K);
+  tp.tiles_m = static_cast<int32_t>(I.grid_m);
+  tp.tiles_n = static_cast<int32_t>(I.grid_n);
+  tp.k_blocks = static_cast<int32_t>(I.k_iters);
+  tp.group_m = static_cast<int32_t>(h->group_m < I.grid_m ? h->group_m : I.grid_m);
+  tp.idesc = make_idesc(P.in_dtype, pl.a.mn_major, pl.b.mn_major, I.tile_n, I.tile_m);
+  tp.out_dtype = P.out_dtype;
+  tp.tma_store = I.tma_store;
+  tp.C = P.C;
+  tp.ldc = P.ldc;
+  tp.status = h->status;
+  tp.timeout_ns = h->timeout_us * 1000ull;
+  tp.debug_flags = h->stall_producer ? kDebugStallProducer : 0;
+  e = tc_launch(pl.variant, tmA, tmB, tmC, tp, static_cast<int>(I.ctas), s);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 launch");
+  h->launches += 1;
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_API const char *gemm_version(void) { return kVersion; }
+
+GEMM_API const char *gemm_strerror(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "success";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported request";
+    case GEMM_ERR_ALIGNMENT: return "pointer not aligned to its element size";
+    case GEMM_ERR_NO_MEMORY: return "workspace allocation failed";
+    case GEMM_ERR_CUDA: return "CUDA call failed";
+    case GEMM_ERR_TIMEOUT: return "device-side bounded wait expired";
+    case GEMM_ERR_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+GEMM_API gemm_status_t gemm_create(gemm_handle_t *out, int device) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_DEVICE;
+  }
+  if (device < 0 || device >= n) return GEMM_ERR_DEVICE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_DEVICE;  // built for sm_103a only
+  DeviceGuard g(device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  gemm_handle_t h = new (std::nothrow) gemm_handle_s();
+  if (!h) return GEMM_ERR_NO_MEMORY;
+  h->device = device;
+  h->sm_count = prop.multiProcessorCount;
+  if (cudaMalloc(&h->status, sizeof(int)) != cudaSuccess ||
+      cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->status) cudaFree(h->status);
+    delete h;
+    return GEMM_ERR_NO_MEMORY;
+  }
+  *out = h;
+  return GEMM_OK;
+}
+
+GEMM_API void gemm_destroy(gemm_handle_t h) {
+  if (!h) return;
+  DeviceGuard g(h->device);
+  cudaDeviceSynchronize();
+  if (h->workspace) cudaFree(h->workspace);
+  if (h->status) cudaFree(h->status);
+  delete h;
+}
+
+GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t v) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  switch (opt) {
+    case GEMM_OPT_WAIT_TIMEOUT_US:
+      if (v < 1 || v > 600000000) return GEMM_ERR_INVALID_ARG;
+      h->timeout_us = static_cast<uint64_t>(v);
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_PATH:
+      if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
+      h->force_path = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_GROUP_M:
+      if (v < 1 || v > 65536) return GEMM_ERR_INVALID_ARG;
+      h->group_m = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_MAX_CTAS:
+      if (v < 0 || v > 1 << 20) return GEMM_ERR_INVALID_ARG;
+      h->max_ctas = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_FAULT_STALL_PRODUCER:
+      if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
+      h->stall_producer = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_STAGING:
+      if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
+      h->force_staging = static_cast<int>(v);
+      return GEMM_OK;
+  }
+  return GEMM_ERR_INVALID_ARG;
+}
+
+GEMM_API gemm_status_t gemm_get_launch_count(gemm_handle_t h, uint64_t *count) {
+  if (!h || !count) return GEMM_ERR_INVALID_ARG;
+  *count = h->launches;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+                                 int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
+                                 gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+                                 gemm_precision_t precision_mode, gemm_layout_t a_layout,
+                                 gemm_layout_t b_layout, int32_t sm_count, gemm_plan_info_t *info) {
+  if (!info) return GEMM_ERR_INVALID_ARG;
+  const Problem P{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
+                  b_layout};
+  Plan pl;
+  gemm_status_t st = make_plan(P, options_of(h), sm_count, &pl);
+  if (st == GEMM_OK) *info = pl.info;
+  return st;
+}
+
+GEMM_API gemm_status_t gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                   const void *A, int64_t lda, const void *B, int64_t ldb,
+                                   void *C, int64_t ldc, gemm_dtype_t in_dtype,
+                                   gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
+                                   gemm_layout_t a_layout, gemm_layout_t b_layout,
+                                   void *cuda_stream) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  const Problem P{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
+                  b_layout};
+  Plan pl;
+  gemm_status_t st = make_plan(P, options_of(h), h->sm_count, &pl);
+  if (st != GEMM_OK) return st;
+  DeviceGuard g(h->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  return execute(h, P, pl, static_cast<cudaStream_t>(cuda_stream));
+}
+
+GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+                                int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
+                                gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+                                gemm_precision_t precision_mode) {
+  return gemm_run_ex(h, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode,
+                     GEMM_ROW_MAJOR, GEMM_ROW_MAJOR, nullptr);
+}
+
+GEMM_API gemm_status_t gemm_get_status(gemm_handle_t h, void *cuda_stream) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, h->status, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (word != 0) {
+    e = cudaMemset(h->status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    return static_cast<gemm_status_t>(word);
+  }
+  return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// internal.h -- declarations shared by the host runtime (gemm_api.cu) and the kernel
+// translation units. Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm.h"
+
+namespace gemm_gb300 {
+
+// Debug flags carried into the tensor-core kernel.
+enum : int { kDebugStallProducer = 1 };
+
+// Output tile of the tensor-core kernel: 128 rows (one TMEM lane per row).
+constexpr int kTcBlockM = 128;
+
+// Arguments of the persistent tensor-core kernel that are not tensor maps.
+struct TcParams {
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, k_blocks;
+  int32_t group_m;     // tile rows per raster group
+  uint32_t idesc;      // tcgen05 instruction descriptor
+  int32_t out_dtype;   // gemm_dtype_t
+  int32_t tma_store;   // 1: TMA-store epilogue; 0: masked st.global epilogue
+  void *C;
+  int64_t ldc;
+  int *status;         // device status word
+  uint64_t timeout_ns; // bounded-wait limit
+  int32_t debug_flags;
+};
+
+// One tensor-core kernel variant: element size of A and B (2 = f16/bf16, 4 = fp32 as tf32),
+// operand majorness, and the output tile width.
+struct TcVariant {
+  int esize;
+  bool a_mn, b_mn;
+  int block_n;
+};
+
+int tc_stages(const TcVariant &v);
+size_t tc_smem_bytes(const TcVariant &v);
+cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                      const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+
+// fp32 fused-multiply-add tile kernel (exact fp32 mode; any input dtype/layout).
+struct FmaParams {
+  int64_t M, N, K;
+  const void *A;
+  int64_t lda;
+  const void *B;
+  int64_t ldb;
+  void *C;
+  int64_t ldc;
+  int32_t in_dtype, out_dtype;
+  int32_t a_col, b_col;  // 1 = column-major operand
+};
+// tile: 4 selects the 4x4x4 tiles of the pages' 8x8x8 example, anything else 128x128x8.
+cudaError_t fma_launch(const FmaParams &p, int tile, cudaStream_t s);
+void fma_tile_shape(int tile, int *bm, int *bn, int *bk);
+
+// Copy a rows x cols operand (storage: `outer` lines of `inner` elements, leading dim
+// ld_src) into dst with leading dim ld_dst. esize is 2 or 4 bytes.
+cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                          int64_t outer, int64_t inner, int esize, cudaStream_t s);
+
+// C[i, j] = 0 for i < M, j < N.
+cudaError_t zero_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, int out_dtype,
+                             cudaStream_t s);
+
+}  // namespace gemm_gb300

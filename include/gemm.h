@@ -1,0 +1,192 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) blocked matrix-multiply library.
+ *
+ * The library computes the blocked matrix multiply of "Chapter 13: The Blocked
+ * Matmul Kernel" (section 13.1, Worked Example 13.1.1):
+ *
+ *     C[M,N] = A[M,K] @ B[K,N],
+ *
+ * as a 2D grid of output tiles, each accumulating its K-loop of partial
+ * products into an fp32 accumulator initialised once (section 13.1, the
+ * "common trap" on where the accumulator is initialised), with every
+ * out-of-range M, N and K element contributing exactly zero (section 13.2,
+ * three-way masking; "Triton from zero, Lesson 4: Block Pointers", section 3,
+ * zero padding), the result rounded once to the output type at the store
+ * (section 13.3), and an explicit choice between tf32 and exact fp32 for fp32
+ * inputs ("Triton matmul", the "Precision" section).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers A, B, C are DEVICE pointers owned by the caller; the library never
+ * frees or retains them past the call. Leading dimensions are in ELEMENTS.
+ *   A: M x K; GEMM_ROW_MAJOR -> A[i,k] at A + i*lda + k (lda >= K);
+ *             GEMM_COL_MAJOR -> A[i,k] at A + k*lda + i (lda >= M).
+ *   B: K x N; GEMM_ROW_MAJOR -> B[k,j] at B + k*ldb + j (ldb >= N);
+ *             GEMM_COL_MAJOR -> B[k,j] at B + j*ldb + k (ldb >= K)
+ *             (the [N,K] storage of the transposed-B read of "Triton from
+ *             zero, Lesson 4", homework 2).
+ *   C: M x N, always row-major: C[i,j] at C + i*ldc + j (ldc >= N).
+ * Only C[i,j] with i < M and j < N is written; bytes of C outside that set
+ * (row tails when ldc > N) are left untouched. A and B are read only inside
+ * their logical extents.
+ *
+ * Arithmetic: products are accumulated in fp32 and rounded once to out_dtype
+ * with round-to-nearest-even. K == 0 writes zeros (the empty sum). M == 0 or
+ * N == 0 is a no-op returning GEMM_OK.
+ *
+ * Precision (fp32 inputs only): GEMM_PREC_DEFAULT means GEMM_PREC_EXACT_FP32
+ * (fp32 fused multiply-adds); GEMM_PREC_TF32 runs the tensor cores on tf32
+ * operands (the low 13 mantissa bits of each fp32 input are ignored). 16-bit
+ * inputs accept only GEMM_PREC_DEFAULT.
+ *
+ * Errors: checks on the host return a status and launch nothing. Work is
+ * asynchronous on the given stream, so a GEMM_OK return means "launched";
+ * faults found by the device (a bounded wait that expired) are reported by
+ * gemm_get_status. A misaligned pointer or leading dimension is not an error:
+ * the library stages such an operand through an aligned workspace that the
+ * handle owns.
+ *
+ * Threads and streams: a handle may be used from one host thread at a time.
+ * Its workspace is reused by every call, so two calls on one handle that may
+ * run concurrently on the GPU (different streams, no ordering) must not both
+ * need the workspace; calls on a single stream are always safe.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+typedef struct gemm_handle_s *gemm_handle_t;
+
+typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2 } gemm_dtype_t;
+
+typedef enum {
+  GEMM_PREC_DEFAULT = 0,   /* exact fp32 for fp32 inputs; the only mode for 16-bit inputs */
+  GEMM_PREC_TF32 = 1,      /* fp32 inputs on the tf32 tensor-core path */
+  GEMM_PREC_EXACT_FP32 = 2 /* fp32 inputs, fp32 fused multiply-add accumulation */
+} gemm_precision_t;
+
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1, /* null/negative/overlapping/too-small argument */
+  GEMM_ERR_UNSUPPORTED = 2, /* a valid request this library does not implement */
+  GEMM_ERR_ALIGNMENT = 3,   /* a pointer not aligned to its element size */
+  GEMM_ERR_NO_MEMORY = 4,   /* workspace allocation failed */
+  GEMM_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+  GEMM_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (see gemm_get_status) */
+  GEMM_ERR_DEVICE = 7       /* no usable sm_103 device */
+} gemm_status_t;
+
+/* Create a handle bound to CUDA device `device`. On success *out receives the
+ * handle (free it with gemm_destroy). Allocates the device status word.
+ * Errors: INVALID_ARG (out == NULL), DEVICE (no such device or not sm_103),
+ * CUDA, NO_MEMORY. */
+GEMM_API gemm_status_t gemm_create(gemm_handle_t *out, int device);
+
+/* Free the handle, its workspace and its status word. Synchronises the device
+ * first so no launched work still uses the workspace. NULL is a no-op. */
+GEMM_API void gemm_destroy(gemm_handle_t h);
+
+/* C = A @ B with row-major A and B on the legacy default stream.
+ * Same as gemm_run_ex(..., GEMM_ROW_MAJOR, GEMM_ROW_MAJOR, NULL). */
+GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                const void *A, int64_t lda, const void *B, int64_t ldb,
+                                void *C, int64_t ldc, gemm_dtype_t in_dtype,
+                                gemm_dtype_t out_dtype, gemm_precision_t precision_mode);
+
+/* C = A @ B with explicit operand layouts, enqueued on `cuda_stream` (a
+ * cudaStream_t; NULL = legacy default stream). The host-side planner picks the
+ * kernel (tcgen05 tensor-core path for 16-bit inputs and tf32 mode, fp32 FMA
+ * path for exact mode), stages misaligned operands, and launches.
+ * Errors (nothing launched): INVALID_ARG for h == NULL, negative sizes, a null
+ * pointer with a non-empty extent, a leading dimension below its minimum, an
+ * unknown enum, or C's span overlapping A's or B's; UNSUPPORTED for a
+ * precision other than DEFAULT with 16-bit inputs; ALIGNMENT for a pointer not
+ * aligned to its element size; NO_MEMORY/CUDA from staging or launch. */
+GEMM_API gemm_status_t gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                   const void *A, int64_t lda, const void *B, int64_t ldb,
+                                   void *C, int64_t ldc, gemm_dtype_t in_dtype,
+                                   gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
+                                   gemm_layout_t a_layout, gemm_layout_t b_layout,
+                                   void *cuda_stream);
+
+/* Synchronise `cuda_stream` (NULL = legacy default stream), then read and clear
+ * the handle's device status word. Returns GEMM_OK, GEMM_ERR_TIMEOUT when a
+ * kernel's bounded wait expired since the last call (its C is then
+ * undefined), or GEMM_ERR_CUDA when the synchronisation itself failed. */
+GEMM_API gemm_status_t gemm_get_status(gemm_handle_t h, void *cuda_stream);
+
+/* Static description of a status code; never NULL. */
+GEMM_API const char *gemm_strerror(gemm_status_t s);
+
+/* ---------------------------------------------------------------- tuning */
+
+typedef enum {
+  GEMM_OPT_WAIT_TIMEOUT_US = 0, /* device bounded-wait limit in microseconds (default 2000000) */
+  GEMM_OPT_FORCE_PATH = 1,      /* 0 auto, 1 tensor-core path, 2 fp32 FMA path (exact fp32 only) */
+  GEMM_OPT_GROUP_M = 2,         /* tile rows per raster group of the persistent schedule (>= 1) */
+  GEMM_OPT_MAX_CTAS = 3,        /* cap on persistent CTAs (0 = one per SM) */
+  GEMM_OPT_FAULT_STALL_PRODUCER = 4, /* test hook: the tensor-core kernel's loader issues
+                                        nothing, so the consumers' bounded waits expire and the
+                                        kernel reports GEMM_ERR_TIMEOUT; 0 = off */
+  GEMM_OPT_FORCE_STAGING = 5    /* 1 = stage A and B through the workspace even when aligned */
+} gemm_option_t;
+
+/* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
+GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value);
+
+/* Number of kernels this handle has launched since it was created. */
+GEMM_API gemm_status_t gemm_get_launch_count(gemm_handle_t h, uint64_t *count);
+
+/* ------------------------------------------------------------- planning */
+
+typedef enum {
+  GEMM_PATH_NONE = 0,      /* nothing to do (M == 0 or N == 0) */
+  GEMM_PATH_ZERO_FILL = 1, /* K == 0: C is set to zero */
+  GEMM_PATH_TCGEN05 = 2,   /* TMA + mbarrier pipeline + tcgen05.mma, TMEM accumulator */
+  GEMM_PATH_FMA = 3        /* fp32 fused multiply-add tiles (exact fp32 mode) */
+} gemm_path_t;
+
+typedef struct {
+  int32_t path;           /* gemm_path_t */
+  int32_t tile_m, tile_n, tile_k; /* output tile and K-chunk, in elements */
+  int64_t grid_m, grid_n; /* output tiles along M and N */
+  int64_t k_iters;        /* K-chunks per tile: ceil(K / tile_k) */
+  int32_t stages;         /* shared-memory pipeline depth (tensor-core path) */
+  int32_t stage_a, stage_b; /* 1 if the operand is copied to an aligned workspace first */
+  int32_t a_mn_major, b_mn_major; /* operand read M/N-major (1) or K-major (0) */
+  int32_t tma_store;      /* 1 if the epilogue writes C with TMA stores */
+  int64_t ctas;           /* CTAs launched (persistent schedule) */
+  int64_t workspace_bytes; /* workspace the call needs */
+} gemm_plan_info_t;
+
+/* Host-only: the plan gemm_run_ex would use for these arguments on a GPU with
+ * `sm_count` SMs, without touching any device. Same argument checks and
+ * return codes as gemm_run_ex; h may be NULL (default options). */
+GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                 const void *A, int64_t lda, const void *B, int64_t ldb,
+                                 void *C, int64_t ldc, gemm_dtype_t in_dtype,
+                                 gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
+                                 gemm_layout_t a_layout, gemm_layout_t b_layout,
+                                 int32_t sm_count, gemm_plan_info_t *info);
+
+/* Library version as "major.minor.patch". */
+GEMM_API const char *gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

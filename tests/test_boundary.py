@@ -1,0 +1,160 @@
+"""Host-side tests of the C-ABI library: it loads without a GPU, exports every symbol
+include/gemm.h declares, rejects bad arguments before launching anything, and plans
+each workload the way the design says. Nothing here calls a GPU kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import dense_tiled_gemm_05_gb300 as g
+from dense_tiled_gemm_05_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return g.lib()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "gemm.h")).read()
+    return sorted(set(re.findall(r"GEMM_API\s+[\w\s\*]+?\b(gemm_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = header_symbols()
+    assert set(declared) == set(g.EXPORTS), declared
+    for name in declared:
+        assert hasattr(L, name), name
+    # Nothing but the declared API is exported (hidden visibility for internals).
+    out = os.popen("nm -D --defined-only %s" % g.LIB_PATH).read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert {s for s in exported if s.startswith("gemm_")} == set(declared)
+
+
+def test_version_and_strerror(L):
+    assert re.match(r"^\d+\.\d+\.\d+$", g.version())
+    for code in range(8):
+        assert L.gemm_strerror(code)
+    assert L.gemm_strerror(99) == b"unknown status"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_create_without_gpu_reports_device_error(L):
+    h = ctypes.c_void_p()
+    assert L.gemm_create(ctypes.byref(h), 0) == 7  # GEMM_ERR_DEVICE
+    assert h.value is None
+    assert L.gemm_create(None, 0) == 1
+
+
+def test_null_handle_is_rejected(L):
+    assert L.gemm_run(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0) == 1
+    assert L.gemm_get_status(None, None) == 1
+    assert L.gemm_set_option(None, 0, 1) == 1
+    L.gemm_destroy(None)  # no-op
+
+
+def t(shape, dtype, layout="row"):
+    x = torch.zeros(shape[::-1] if layout == "col" else shape, dtype=dtype)
+    return x.t() if layout == "col" else x
+
+
+def test_plan_small_exact_uses_pages_tiles():
+    # The pages' 8x8x8 example: 4x4x4 tiles, grid (2, 2), two K-iterations per tile.
+    p = g.plan(t((8, 8), torch.float32), t((8, 8), torch.float32), precision="exact")
+    assert p["path"] == "fma"
+    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (4, 4, 4)
+    assert (p["grid_m"], p["grid_n"], p["k_iters"]) == (2, 2, 2)
+    assert g.plan(t((8, 8), torch.float32), t((8, 8), torch.float32))["path"] == "fma"
+
+
+def test_plan_bf16_square_is_tcgen05_k_major():
+    p = g.plan(t((4096, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
+               sm_count=148)
+    assert p["path"] == "tcgen05"
+    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 256, 64)
+    assert (p["grid_m"], p["grid_n"], p["k_iters"]) == (32, 16, 64)
+    assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
+    assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["tma_store"] == 1
+    assert p["ctas"] == 148 and p["workspace_bytes"] == 0
+
+
+def test_plan_row_major_b_is_mn_major():
+    p = g.plan(t((256, 512), torch.float16), t((512, 300), torch.float16))
+    assert p["path"] == "tcgen05" and p["b_mn_major"] == 1 and p["a_mn_major"] == 0
+    p = g.plan(t((256, 512), torch.float16, "col"), t((512, 304), torch.float16))
+    assert p["a_mn_major"] == 1 and p["stage_a"] == 0
+
+
+def test_plan_ragged_stages_misaligned_operands():
+    # fp16 with K = 1025: a row is 2050 bytes, not a multiple of 16 -> staged copy.
+    a, b = t((1023, 1025), torch.float16), t((1025, 17), torch.float16)
+    p = g.plan(a, b, out_dtype="f32")
+    assert p["stage_a"] == 1 and p["stage_b"] == 1 and p["tma_store"] == 0
+    assert p["workspace_bytes"] >= 1023 * 1032 * 2 + 1025 * 24 * 2
+    # K = 1000 (2000-byte rows) is TMA-legal in place; N = 1000 fp32 C rows are 4000 bytes.
+    p = g.plan(t((17, 1000), torch.float16), t((1000, 1000), torch.float16), out_dtype="f32")
+    assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["tma_store"] == 1
+    # A misaligned base pointer is staged, not rejected.
+    a = t((64, 64), torch.float16)
+    p = g.plan(a, t((64, 64), torch.float16), a_ptr=a.data_ptr() + 2)
+    assert p["stage_a"] == 1
+
+
+def test_plan_fp32_modes():
+    a, b = t((4096, 4096), torch.float32), t((4096, 4096), torch.float32)
+    p = g.plan(a, b, precision="tf32")
+    assert p["path"] == "tcgen05" and p["tile_k"] == 32 and p["k_iters"] == 128
+    for prec in ("exact", "default"):
+        p = g.plan(a, b, precision=prec)
+        assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 128, 8)
+
+
+def test_plan_degenerate_shapes():
+    assert g.plan(t((0, 5), torch.float16), t((5, 7), torch.float16))["path"] == "none"
+    assert g.plan(t((5, 3), torch.float16), t((3, 0), torch.float16))["path"] == "none"
+    assert g.plan(t((5, 0), torch.float16), t((0, 7), torch.float16))["path"] == "zero_fill"
+
+
+def plan_code(L, M, N, K, A, lda, B, ldb, C, ldc, in_dt=1, out_dt=0, prec=0, al=0, bl=0):
+    info = g.PlanInfo()
+    return L.gemm_plan(None, M, N, K, A, lda, B, ldb, C, ldc, in_dt, out_dt, prec, al, bl, 148,
+                       ctypes.byref(info))
+
+
+def test_plan_rejects_bad_arguments(L):
+    A, B, C = 1 << 20, 1 << 24, 1 << 28
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16) == 0
+    assert plan_code(L, -1, 16, 16, A, 16, B, 16, C, 16) == 1        # negative size
+    assert plan_code(L, 16, 16, 16, A, 15, B, 16, C, 16) == 1        # lda < K
+    assert plan_code(L, 16, 16, 16, A, 16, B, 15, C, 16) == 1        # ldb < N
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 15) == 1        # ldc < N
+    assert plan_code(L, 16, 16, 16, A, 8, B, 16, C, 16, al=1) == 1   # col-major A: lda < M
+    assert plan_code(L, 16, 16, 16, None, 16, B, 16, C, 16) == 1     # null A
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, None, 16) == 1     # null C
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, in_dt=7) == 1
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, al=3) == 1
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, prec=1) == 2  # tf32 with fp16 in
+    assert plan_code(L, 16, 16, 16, A + 1, 16, B, 16, C, 16) == 3      # odd fp16 address
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C + 2, 16) == 3      # fp32 C at 2 bytes
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, A + 64, 16) == 1     # C overlaps A
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, B - 16, 16) == 1     # C overlaps B
+    assert plan_code(L, 0, 16, 16, None, 16, None, 16, None, 16) == 0  # empty: nothing needed
+    assert plan_code(L, 16, 16, 0, None, 16, None, 16, C, 16) == 0     # K == 0: only C needed
+
+
+def test_sources_share_nothing_with_the_oracle():
+    csrc = os.path.join(ROOT, "dense_tiled_gemm_05_gb300")
+    for dirpath, _, files in os.walk(csrc):
+        for f in files:
+            if f.endswith((".cu", ".cuh", ".h", ".py", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".c", ".py")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "dense_tiled_gemm_05_gb300" not in text and "gemm.h" not in text, f

@@ -1,0 +1,69 @@
+"""Failure detection on the GPU without a GPU fault: the tensor-core kernel's loader
+is told to issue nothing, so the MMA and epilogue roles' bounded mbarrier waits expire
+after a short limit; the kernel records GEMM_ERR_TIMEOUT in the handle's status word,
+releases its TMEM and returns. The same context then runs a normal GEMM correctly."""
+import pytest
+import torch
+
+import workloads as W
+from gpu_util import oracle_rows, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import dense_tiled_gemm_05_gb300 as g
+    g.build.build()
+    return g
+
+
+def test_bounded_wait_expires_and_context_stays_usable(g):
+    p = W.bf16_square(512)
+    a, b = to_device(p.A), to_device(p.B)
+    h = g.Gemm(0)
+    h.set_option("wait_timeout_us", 20000)  # 20 ms
+    h.set_option("fault_stall_producer", 1)
+    h.matmul(a, b)  # launches; the failure is found on the device
+    assert h.status() == 6  # GEMM_ERR_TIMEOUT
+    assert h.status() == 0  # reading the status clears it
+    h.set_option("fault_stall_producer", 0)
+    c = h.matmul(a, b)
+    assert h.status() == 0
+    C64, D = oracle_rows(p)
+    assert rel_err(c, C64, D) <= 1e-2
+    h.close()
+
+
+def test_timeout_then_other_handles_unaffected(g):
+    p = W.integer_problem(300, 400, 500, "f16", seed=3)
+    a, b = to_device(p.A), to_device(p.B)
+    bad, good = g.Gemm(0), g.Gemm(0)
+    bad.set_option("wait_timeout_us", 10000)
+    bad.set_option("fault_stall_producer", 1)
+    bad.matmul(a, b, out_dtype="f32")
+    c = good.matmul(a, b, out_dtype="f32")
+    assert bad.status() == 6
+    assert good.status() == 0
+    assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    bad.close()
+    good.close()
+
+
+def test_workspace_allocation_failure_is_reported(g, monkeypatch):
+    # Host-side fault injection: the staging workspace cannot be allocated.
+    monkeypatch.setenv("GEMM_FAULT_INJECT", "alloc")
+    p = W.ragged(127, 17, 1025)  # misaligned rows: needs the staging workspace
+    a, b = to_device(p.A), to_device(p.B)
+    h = g.Gemm(0)
+    with pytest.raises(g.GemmError) as e:
+        h.matmul(a, b, out_dtype="f32")
+    assert e.value.code == 4  # GEMM_ERR_NO_MEMORY
+    monkeypatch.delenv("GEMM_FAULT_INJECT")
+    c = h.matmul(a, b, out_dtype="f32")
+    assert h.status() == 0
+    C64, D = oracle_rows(p)
+    assert rel_err(c, C64, D) <= 1e-2
+    h.close()

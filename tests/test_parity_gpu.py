@@ -1,0 +1,278 @@
+"""GPU parity: the library (through its C ABI) against the CPU oracle, element by
+element on the seeded workloads, on every kernel path, layout and dtype, plus the
+edge cases of the method (ragged M/N/K, K == 0, empty outputs, padded and
+misaligned operands, untouched bytes outside C, determinism)."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_util import (check_sampled, check_sums, oracle_rows, rel_err, run_gpu, to_device,
+                      tolerance)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import dense_tiled_gemm_05_gb300 as g
+    g.build.build()
+    return g.Gemm(0)
+
+
+def full_check(h, p, **kw):
+    c = run_gpu(h, p, **kw)
+    C64, D = oracle_rows(p)
+    err = rel_err(c, C64, D)
+    assert err <= tolerance(p), "%s: rel err %.3g > %.3g" % (p.name, err, tolerance(p))
+    return c, err
+
+
+# ------------------------------------------------------------ the pages' cases
+
+@pytest.mark.parametrize("dtype,precision", [("f32", "exact"), ("f16", "default"),
+                                             ("bf16", "default"), ("f32", "tf32")])
+def test_two_by_two(h, dtype, precision):
+    p = W.two_by_two(dtype)
+    p.precision = precision
+    p.out_dtype = "f32"
+    c = run_gpu(h, p)
+    assert c.cpu().tolist() == [[19.0, 22.0], [43.0, 50.0]]
+
+
+def test_small_exact_8x8x8_on_4x4x4_tiles(h):
+    p = W.small_exact()
+    plan = h.plan(to_device(p.A), to_device(p.B), out_dtype="f32", precision="exact")
+    assert (plan["tile_m"], plan["grid_m"], plan["grid_n"], plan["k_iters"]) == (4, 2, 2, 2)
+    full_check(h, p)
+
+
+@pytest.mark.parametrize("M,K,N", [(8, 8, 8), (5, 7, 6)])
+@pytest.mark.parametrize("dtype,precision", [("f32", "exact"), ("f32", "tf32"),
+                                             ("f16", "default")])
+def test_arange_examples(h, M, K, N, dtype, precision):
+    p = W.arange_tenths(M, K, N, dtype)
+    p.precision, p.out_dtype = precision, "f32"
+    full_check(h, p)
+
+
+@pytest.mark.parametrize("dtype,precision", [("f32", "exact"), ("f32", "tf32"),
+                                             ("f16", "default"), ("bf16", "default")])
+def test_sentinel_k_mask(h, dtype, precision):
+    # Operands sliced from parents whose k >= 5 columns/rows hold 999: the library must
+    # read none of them (the missing-K-mask failure would add ~2,994,003 everywhere).
+    p = W.sentinel_padded(dtype=dtype)
+    p.precision, p.out_dtype = precision, "f32"
+    c, _ = full_check(h, p)
+    assert float(c.abs().max()) < 20.0
+
+
+# ----------------------------------------------------------------- ragged sweep
+
+def test_ragged_sweep_all_216(h):
+    worst, failures = 0.0, []
+    for (M, N, K) in W.ragged_combos():
+        p = W.ragged(M, N, K)
+        c = run_gpu(h, p)
+        C64, D = oracle_rows(p)
+        err = rel_err(c, C64, D)
+        worst = max(worst, err)
+        if err > tolerance(p):
+            failures.append(((M, N, K), err))
+    assert not failures, failures[:10]
+    assert worst < 1e-2
+
+
+@pytest.mark.parametrize("M,N,K", [(1025, 17, 1023), (127, 1000, 1025), (17, 1023, 1000),
+                                   (1, 1025, 127)])
+def test_ragged_guard_bands(h, M, N, K):
+    # A and B live in padded parents whose tails hold 999; C lives in a NaN-filled parent
+    # with a wider row pitch. The result must equal the zero-tailed run bit for bit and
+    # every byte of C's parent outside [0, M) x [0, N) must keep its NaN pattern.
+    seed = 7 * M + N + K
+    results = []
+    for tail in (0.0, 999.0):
+        A = W.make_operand(M, K, "f16", "row", seed, ld_pad=13)
+        B = W.make_operand(K, N, "f16", "row", seed + 1, ld_pad=9)
+        A.as_strided((M, 13), (A.stride(0), 1), A.storage_offset() + K).fill_(tail)
+        B.as_strided((K, 9), (B.stride(0), 1), B.storage_offset() + N).fill_(tail)
+        # C at an odd offset and pitch (plain-store epilogue), then at a 16-byte aligned
+        # offset and pitch (TMA-store epilogue, clipped by the tensor map).
+        for col0, pitch in ((2, N + 5), (4, (N + 8 + 3) // 4 * 4)):
+            parent = torch.full((M + 2, pitch), float("nan"), dtype=torch.float32, device="cuda")
+            out = parent[1:M + 1, col0:col0 + N]
+            c = run_gpu(h, W.Problem("guard", A, B, "f32"), out=out)
+            mask = torch.ones_like(parent, dtype=torch.bool)
+            mask[1:M + 1, col0:col0 + N] = False
+            assert torch.isnan(parent[mask]).all()
+            results.append(c.cpu())
+        if tail == 999.0:
+            C64, D = oracle_rows(W.Problem("guard", A, B, "f32"))
+            assert rel_err(c, C64, D) <= 1e-2
+    assert all(torch.equal(results[0], r) for r in results[1:])
+
+
+# --------------------------------------------------- integer exactness (P7)
+
+INT_SHAPES = [(1, 1, 1), (128, 256, 64), (129, 257, 65), (300, 520, 1025), (777, 33, 200),
+              (64, 600, 8), (1000, 1000, 17)]
+
+
+@pytest.mark.parametrize("dtype,precision", [("bf16", "default"), ("f16", "default"),
+                                             ("f32", "tf32"), ("f32", "exact")])
+@pytest.mark.parametrize("a_layout,b_layout", list(itertools.product(["row", "col"], repeat=2)))
+def test_integer_inputs_bit_exact(h, dtype, precision, a_layout, b_layout):
+    for n, (M, N, K) in enumerate(INT_SHAPES):
+        p = W.integer_problem(M, N, K, dtype, seed=100 + n, a_layout=a_layout,
+                              b_layout=b_layout, precision=precision, ld_pad=n % 3)
+        c = run_gpu(h, p)
+        ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
+        assert torch.equal(c.cpu().to(torch.int64), ref), (M, N, K)
+        assert torch.equal(c.cpu(), ref.to(torch.float32))
+
+
+@pytest.mark.parametrize("out_dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
+def test_output_dtypes_round_once(h, in_dtype, out_dtype):
+    # Integer inputs keep the fp32 accumulator exact; the only rounding is the final one,
+    # round-to-nearest-even into the output type.
+    p = W.integer_problem(300, 260, 1000, in_dtype, seed=5, out_dtype=out_dtype)
+    c = run_gpu(h, p)
+    exact = (p.A.to(torch.int64) @ p.B.to(torch.int64)).to(torch.float64)
+    expect = exact.to(torch.float32).to(W.TORCH_DTYPES[out_dtype])
+    assert c.dtype == W.TORCH_DTYPES[out_dtype]
+    assert torch.equal(c.cpu(), expect)
+
+
+def test_accumulation_precision_example(h):
+    # fp16 in, fp32 accumulate, fp16 out (the chapter's 4 x 1024 x 4 comparison): one
+    # rounding at the store, so the result is the fp16 rounding of the fp32 sum.
+    import oracle
+    p = W.accumulation_13_3_1()
+    c = run_gpu(h, p).double().cpu().numpy()
+    C64, _ = oracle_rows(p)
+    r16 = oracle.round_to(C64, "f16")
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(C64), 2.0 ** -14))) - 10)
+    assert np.all(np.abs(c - r16) <= ulp)  # at most one fp16 step from the exact rounding
+    assert np.max(np.abs(c - C64)) <= 9.737179152580211e-05 + ulp.max()
+
+
+# --------------------------------------------------------- degenerate shapes
+
+def test_k_zero_writes_zeros_and_empty_is_noop(h):
+    a = torch.empty(37, 0, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty(0, 45, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((37, 45), float("nan"), dtype=torch.float32, device="cuda")
+    h.matmul(a, b, out=out)
+    assert h.status() == 0
+    assert torch.equal(out, torch.zeros_like(out)) and not torch.signbit(out).any()
+    out2 = torch.full((0, 45), 1.0, device="cuda")
+    h.matmul(torch.empty(0, 8, dtype=torch.float16, device="cuda"),
+             torch.empty(8, 45, dtype=torch.float16, device="cuda"), out=out2)
+    assert h.status() == 0
+
+
+def test_misaligned_operands_are_staged(h):
+    # Operands starting 2 bytes past an aligned address: TMA cannot read them in place.
+    M, N, K = 200, 300, 260
+    for n, (al, bl) in enumerate(itertools.product(["row", "col"], repeat=2)):
+        p = W.integer_problem(M, N, K, "bf16", seed=40 + n, a_layout=al, b_layout=bl)
+        a = to_device(p.A)
+        b = to_device(p.B)
+        abuf = torch.empty(a.numel() + 8, dtype=a.dtype, device="cuda")
+        bbuf = torch.empty(b.numel() + 8, dtype=b.dtype, device="cuda")
+        a2 = torch.as_strided(abuf, a.shape, a.stride(), 1)
+        b2 = torch.as_strided(bbuf, b.shape, b.stride(), 1)
+        a2.copy_(a)
+        b2.copy_(b)
+        plan = h.plan(a2, b2, out_dtype="f32")
+        assert plan["stage_a"] == 1 and plan["stage_b"] == 1
+        c = h.matmul(a2, b2, out_dtype="f32")
+        assert h.status() == 0
+        ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
+        assert torch.equal(c.cpu().to(torch.int64), ref)
+
+
+# ------------------------------------------------- schedule and determinism
+
+def test_schedule_options_do_not_change_bits(h):
+    import dense_tiled_gemm_05_gb300 as g
+    p = W.bf16_square(1024)
+    a, b = to_device(p.A), to_device(p.B)
+    base = h.matmul(a, b)
+    assert h.status() == 0
+    for opts in ({"max_ctas": 3}, {"group_m": 1}, {"group_m": 5, "max_ctas": 17},
+                 {"force_staging": 1}):
+        h2 = g.Gemm(0)
+        for k, v in opts.items():
+            h2.set_option(k, v)
+        c = h2.matmul(a, b)
+        assert h2.status() == 0
+        assert torch.equal(c, base), opts
+        h2.close()
+    C64, D = oracle_rows(p)
+    assert rel_err(base, C64, D) <= 1e-2
+
+
+def test_mid_size_full_compare_many_tiles_per_cta(h):
+    import dense_tiled_gemm_05_gb300 as g
+    h2 = g.Gemm(0)
+    h2.set_option("max_ctas", 7)  # about 20 tiles per CTA: both TMEM buffers, many phases
+    for p in (W.integer_problem(2048, 1100, 1000, "bf16", seed=9, b_layout="col"),
+              W.integer_problem(1500, 1024, 700, "f32", seed=10, precision="tf32")):
+        c = run_gpu(h2, p)
+        ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
+        assert torch.equal(c.cpu().to(torch.int64), ref)
+    h2.close()
+
+
+def test_deterministic(h):
+    p = W.bf16_square(2048)
+    a, b = to_device(p.A), to_device(p.B)
+    c1 = h.matmul(a, b)
+    c2 = h.matmul(a, b)
+    assert h.status() == 0
+    assert torch.equal(c1, c2)
+
+
+# ------------------------------------------------------- full-size configs
+
+def test_bf16_4096_col_major_b(h):
+    p = W.bf16_square(4096)
+    c = run_gpu(h, p)
+    err = check_sampled(p, c)
+    assert err <= tolerance(p), err
+    s_err, tol = check_sums(p, c)
+    assert s_err <= tol, s_err
+
+
+@pytest.mark.parametrize("precision", ["tf32", "exact"])
+def test_fp32_4096_modes(h, precision):
+    p = W.fp32_square(4096, precision)
+    c = run_gpu(h, p)
+    err = check_sampled(p, c)
+    assert err <= tolerance(p), (precision, err)
+    s_err, tol = check_sums(p, c)
+    assert s_err <= tol, s_err
+
+
+def test_bf16_8192(h):
+    p = W.bf16_square(8192, seed=5)
+    c = run_gpu(h, p)
+    err = check_sampled(p, c, rows=None)
+    assert err <= tolerance(p), err
+    s_err, tol = check_sums(p, c)
+    assert s_err <= tol, s_err
+
+
+def test_bf16_skinny(h):
+    p = W.bf16_skinny()
+    c = run_gpu(h, p)
+    err = check_sampled(p, c)
+    assert err <= tolerance(p), err
+    s_err, tol = check_sums(p, c)
+    assert s_err <= tol, s_err
