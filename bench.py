@@ -160,11 +160,15 @@ def cpu_baseline(p, target_s=10.0):
     b, bl, ldb = W.storage_numpy(p.B)
     kw = dict(lda=lda, ldb=ldb, a_dtype=p.in_dtype, b_dtype=W.dtype_name(p.B.dtype),
               a_layout=al, b_layout=bl)
-    rows = 8
-    t0 = time.perf_counter()
-    oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=np.arange(rows), **kw)
-    t_probe = time.perf_counter() - t0
-    rows = int(max(8, min(p.M, rows * target_s / max(t_probe, 1e-3))))
+    # Calibrate: the per-call cost is a fixed part (decoding B) plus a per-row part.
+    times = {}
+    for r in (4, 12):
+        t0 = time.perf_counter()
+        oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=np.arange(r), **kw)
+        times[r] = time.perf_counter() - t0
+    per_row = max((times[12] - times[4]) / 8, 1e-6)
+    fixed = max(times[4] - 4 * per_row, 0.0)
+    rows = int(max(8, min(p.M, (target_s - fixed) / per_row)))
     sel = np.linspace(0, p.M - 1, rows).astype(np.int64)
     t0 = time.perf_counter()
     oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=sel, **kw)

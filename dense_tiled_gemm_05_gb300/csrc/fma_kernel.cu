@@ -1,4 +1,4 @@
-// fma_kernel.cu -- exact-fp32 tile kernel, operand staging and zero fill.
+// fma_kernel.cu -- exact-fp32 tile kernel, operand staging (copy or transpose) and zero fill.
 //
 // The FMA kernel is the blocked matrix multiply of "Chapter 13: The Blocked Matmul
 // Kernel", section 13.1, Worked Example 13.1.1, done with fp32 fused multiply-adds:
@@ -133,6 +133,31 @@ __global__ void repack_kernel(const T *__restrict__ src, int64_t ld_src, T *__re
       dst[o * ld_dst + x] = src[o * ld_src + x];
 }
 
+// dst[x * ld_dst + o] = src[o * ld_src + x]: `outer` source lines of `inner` elements
+// become `inner` lines of `outer` elements, through 32 x 32 shared-memory tiles so both
+// the reads and the writes are coalesced.
+template <typename T>
+__global__ void transpose_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
+                                 int64_t ld_dst, int64_t outer, int64_t inner) {
+  __shared__ T tile[32][33];
+  for (int64_t o0 = static_cast<int64_t>(blockIdx.y) * 32; o0 < outer;
+       o0 += static_cast<int64_t>(gridDim.y) * 32) {
+    for (int64_t x0 = static_cast<int64_t>(blockIdx.x) * 32; x0 < inner;
+         x0 += static_cast<int64_t>(gridDim.x) * 32) {
+      for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+        const int64_t o = o0 + j, x = x0 + threadIdx.x;
+        if (o < outer && x < inner) tile[j][threadIdx.x] = src[o * ld_src + x];
+      }
+      __syncthreads();
+      for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+        const int64_t x = x0 + j, o = o0 + threadIdx.x;
+        if (x < inner && o < outer) dst[x * ld_dst + o] = tile[threadIdx.x][j];
+      }
+      __syncthreads();
+    }
+  }
+}
+
 template <typename T>
 __global__ void zero_fill_kernel(T *C, int64_t ldc, int64_t M, int64_t N) {
   for (int64_t i = blockIdx.y; i < M; i += gridDim.y)
@@ -174,6 +199,23 @@ cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld
     repack_kernel<uint32_t><<<grid, threads, 0, s>>>(static_cast<const uint32_t *>(src), ld_src,
                                                      static_cast<uint32_t *>(dst), ld_dst, outer,
                                                      inner);
+  return cudaGetLastError();
+}
+
+cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                             int64_t outer, int64_t inner, int esize, cudaStream_t s) {
+  const dim3 block(32, 8);
+  const int64_t gx = (inner + 31) / 32, gy = (outer + 31) / 32;
+  const dim3 grid(static_cast<unsigned>(gx < 4096 ? (gx < 1 ? 1 : gx) : 4096),
+                  static_cast<unsigned>(gy < 4096 ? (gy < 1 ? 1 : gy) : 4096));
+  if (esize == 2)
+    transpose_kernel<uint16_t><<<grid, block, 0, s>>>(static_cast<const uint16_t *>(src), ld_src,
+                                                      static_cast<uint16_t *>(dst), ld_dst, outer,
+                                                      inner);
+  else
+    transpose_kernel<uint32_t><<<grid, block, 0, s>>>(static_cast<const uint32_t *>(src), ld_src,
+                                                      static_cast<uint32_t *>(dst), ld_dst, outer,
+                                                      inner);
   return cudaGetLastError();
 }
 

@@ -120,16 +120,20 @@ struct Options {
 };
 
 // An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
-// elements with leading dimension ld (in elements), possibly staged into the workspace.
+// elements with leading dimension ld (in elements). It is either read in place or staged
+// into the workspace first: copied when TMA cannot address it (misaligned base or
+// leading dimension), or transposed into K-major form when it is an MN-major tf32
+// operand (the tf32 tensor-core instruction reads K-major operands only).
 struct OperandPlan {
-  const void *ptr;
-  int64_t ld, outer, inner;
-  bool mn_major;
-  bool staged;
+  const void *ptr;          // caller's operand
+  int64_t ld, outer, inner; // caller's storage: outer lines of inner elements
+  bool staged, transpose;
   int64_t staged_ld;
   size_t ws_offset, ws_bytes;
+  // as read by the kernel (after staging)
+  bool mn_major;
+  int64_t k_outer, k_inner;
 };
-
 struct Plan {
   gemm_plan_info_t info;
   TcVariant variant;
@@ -198,11 +202,19 @@ OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, 
   // The operand is K-major when K is its contiguous axis.
   const bool k_inner = k_is_rows_dim ? layout == GEMM_COL_MAJOR : layout == GEMM_ROW_MAJOR;
   o.mn_major = !k_inner;
-  o.staged = force_stage || !tma_legal(p, ld, o.outer, es);
+  o.k_outer = o.outer;
+  o.k_inner = o.inner;
+  o.transpose = o.mn_major && es == 4;
+  o.staged = o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
   if (o.staged) {
-    o.staged_ld = round_up(o.inner, 16 / es);
+    if (o.transpose) {
+      o.k_outer = o.inner;
+      o.k_inner = o.outer;
+      o.mn_major = false;
+    }
+    o.staged_ld = round_up(o.k_inner, 16 / es);
     o.ws_offset = *ws_cursor;
-    o.ws_bytes = static_cast<size_t>(o.staged_ld * o.outer * es);
+    o.ws_bytes = static_cast<size_t>(o.staged_ld * o.k_outer * es);
     *ws_cursor = static_cast<size_t>(round_up(static_cast<int64_t>(*ws_cursor + o.ws_bytes), 256));
   }
   return o;
@@ -265,7 +277,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   I.stages = tc_stages(pl.variant);
   I.stage_a = pl.a.staged, I.stage_b = pl.b.staged;
   I.a_mn_major = pl.a.mn_major, I.b_mn_major = pl.b.mn_major;
-  I.tma_store = reinterpret_cast<uintptr_t>(P.C) % 16 == 0 && (P.ldc * os) % 16 == 0;
+  // TMA stores need a 16-byte aligned base and row pitch; they are also used only when a
+  // row of C ends on a 16-byte boundary, because a store box clipped at a right edge that
+  // falls inside a 16-byte granule was seen to write the whole granule (past column N).
+  I.tma_store = reinterpret_cast<uintptr_t>(P.C) % 16 == 0 && (P.ldc * os) % 16 == 0 &&
+                (P.N * os) % 16 == 0;
   const int64_t tiles = I.grid_m * I.grid_n;
   int64_t ctas = sm_count > 0 ? sm_count : 1;
   if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
@@ -375,19 +391,17 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   int64_t a_ld = pl.a.ld;
   const void *b_ptr = pl.b.ptr;
   int64_t b_ld = pl.b.ld;
-  if (pl.a.staged) {
-    void *dst = static_cast<char *>(h->workspace) + pl.a.ws_offset;
-    e = repack_launch(pl.a.ptr, pl.a.ld, dst, pl.a.staged_ld, pl.a.outer, pl.a.inner, es, s);
-    if (e != cudaSuccess) return cuda_fail(e, "stage A");
+  for (const OperandPlan *o : {&pl.a, &pl.b}) {
+    if (!o->staged) continue;
+    void *dst = static_cast<char *>(h->workspace) + o->ws_offset;
+    e = o->transpose ? transpose_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s)
+                     : repack_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stage operand");
     h->launches += 1;
-    a_ptr = dst, a_ld = pl.a.staged_ld;
-  }
-  if (pl.b.staged) {
-    void *dst = static_cast<char *>(h->workspace) + pl.b.ws_offset;
-    e = repack_launch(pl.b.ptr, pl.b.ld, dst, pl.b.staged_ld, pl.b.outer, pl.b.inner, es, s);
-    if (e != cudaSuccess) return cuda_fail(e, "stage B");
-    h->launches += 1;
-    b_ptr = dst, b_ld = pl.b.staged_ld;
+    if (o == &pl.a)
+      a_ptr = dst, a_ld = o->staged_ld;
+    else
+      b_ptr = dst, b_ld = o->staged_ld;
   }
   const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
   CUtensorMap tmA, tmB, tmC;
@@ -396,8 +410,10 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   // box = (one 128-byte row of M or N) x (the stage's K rows).
   const uint32_t a_box_outer = pl.a.mn_major ? row_elems : static_cast<uint32_t>(I.tile_m);
   const uint32_t b_box_outer = pl.b.mn_major ? row_elems : static_cast<uint32_t>(I.tile_n);
-  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.inner, pl.a.outer, a_ld, row_elems, a_box_outer) ||
-      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.inner, pl.b.outer, b_ld, row_elems, b_box_outer))
+  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, row_elems,
+                 a_box_outer) ||
+      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
+                 b_box_outer))
     return GEMM_ERR_CUDA;
   if (I.tma_store) {
     const uint32_t out_row = 128 / esize_of(P.out_dtype);

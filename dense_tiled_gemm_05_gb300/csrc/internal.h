@@ -65,6 +65,11 @@ void fma_tile_shape(int tile, int *bm, int *bn, int *bk);
 cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                           int64_t outer, int64_t inner, int esize, cudaStream_t s);
 
+// Transposing copy: source `outer` lines of `inner` elements (leading dim ld_src) become
+// `inner` lines of `outer` elements in dst (leading dim ld_dst >= outer).
+cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                             int64_t outer, int64_t inner, int esize, cudaStream_t s);
+
 // C[i, j] = 0 for i < M, j < N.
 cudaError_t zero_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, int out_dtype,
                              cudaStream_t s);

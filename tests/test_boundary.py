@@ -99,6 +99,10 @@ def test_plan_ragged_stages_misaligned_operands():
     # K = 1000 (2000-byte rows) is TMA-legal in place; N = 1000 fp32 C rows are 4000 bytes.
     p = g.plan(t((17, 1000), torch.float16), t((1000, 1000), torch.float16), out_dtype="f32")
     assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["tma_store"] == 1
+    # A row of C that does not end on a 16-byte boundary is written with plain stores.
+    p = g.plan(t((64, 64), torch.float16), t((64, 17), torch.float16), out_dtype="f32",
+               ldc=28)
+    assert p["tma_store"] == 0
     # A misaligned base pointer is staged, not rejected.
     a = t((64, 64), torch.float16)
     p = g.plan(a, t((64, 64), torch.float16), a_ptr=a.data_ptr() + 2)
@@ -109,6 +113,13 @@ def test_plan_fp32_modes():
     a, b = t((4096, 4096), torch.float32), t((4096, 4096), torch.float32)
     p = g.plan(a, b, precision="tf32")
     assert p["path"] == "tcgen05" and p["tile_k"] == 32 and p["k_iters"] == 128
+    # The tf32 instruction reads K-major operands only: a row-major B is transposed into
+    # the workspace; a row-major A is already K-major and read in place.
+    assert p["stage_a"] == 0 and p["stage_b"] == 1 and p["b_mn_major"] == 0
+    assert p["workspace_bytes"] == 4096 * 4096 * 4
+    p = g.plan(t((100, 60), torch.float32, "col"), t((60, 50), torch.float32, "col"),
+               precision="tf32")
+    assert p["stage_a"] == 1 and p["a_mn_major"] == 0 and p["stage_b"] == 0
     for prec in ("exact", "default"):
         p = g.plan(a, b, precision=prec)
         assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 128, 8)

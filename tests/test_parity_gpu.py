@@ -108,7 +108,9 @@ def test_ragged_guard_bands(h, M, N, K):
             c = run_gpu(h, W.Problem("guard", A, B, "f32"), out=out)
             mask = torch.ones_like(parent, dtype=torch.bool)
             mask[1:M + 1, col0:col0 + N] = False
-            assert torch.isnan(parent[mask]).all()
+            bad = (mask & ~torch.isnan(parent)).nonzero()
+            assert bad.numel() == 0, "C pitch %d offset %d: guard cells written, e.g. %s" % (
+                pitch, col0, bad[:6].tolist())
             results.append(c.cpu())
         if tail == 999.0:
             C64, D = oracle_rows(W.Problem("guard", A, B, "f32"))
