@@ -20,7 +20,8 @@ def h():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     import dense_tiled_gemm_05_gb300 as g
-    g.build.build()
+    from dense_tiled_gemm_05_gb300 import build as gbuild
+    gbuild.build()
     return g.Gemm(0)
 
 
