@@ -40,7 +40,7 @@ _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
-           "gemm_version")
+           "gemm_version", "gemm_run_noalloc")
 
 
 class GemmError(RuntimeError):
@@ -101,6 +101,9 @@ def lib():
                 L.gemm_plan.argtypes = run_args + [i32, i32, ctypes.c_int32,
                                                    ctypes.POINTER(PlanInfo)]
                 L.gemm_plan.restype = i32
+                L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32,
+                                               i32, i32, i32, i32, vp, vp]
+                L.gemm_run_noalloc.restype = i32
                 L.gemm_version.argtypes = []
                 L.gemm_version.restype = ctypes.c_char_p
                 _lib = L

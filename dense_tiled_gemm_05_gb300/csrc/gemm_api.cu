@@ -593,3 +593,163 @@ GEMM_API gemm_status_t gemm_get_status(gemm_handle_t h, void *cuda_stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc at the point where they need a product: code that
+// runs while a framework owns every device allocation (a plugin inside another runtime's
+// memory pool), deployments that reserve all device memory up front and forbid growth,
+// and host callbacks or real-time paths where a cudaMalloc (which may synchronise the
+// device) is not allowed. gemm_run_noalloc serves them without a handle: the staging
+// copies that misaligned operands and MN-major tf32 operands need go to a fixed, file-scope
+// device array instead of a workspace that grows on demand.
+namespace {
+
+constexpr size_t kStaticStatusBytes = 256;  // first 256 bytes: the call's status word
+static_assert(GEMM_NOALLOC_SCRATCH_BYTES > kStaticStatusBytes, "scratch too small");
+
+// Every GPU on which this library's device code is loaded keeps this array until the
+// process exits. All calls on a device share it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+int g_noalloc_sms[kMaxDevices];
+
+// Per-device set-up, done by the first call on each device with that device current:
+// look up the array's device address (host code only has a stand-in symbol for it) and
+// the SM count. Later calls reuse both.
+gemm_status_t noalloc_setup(int dev, void **scratch, int *sms) {
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    int major = 0, minor = 0, count = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_DEVICE;
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "look up the static scratch");
+    g_noalloc_sms[dev] = count;
+    g_noalloc_ptr[dev] = p;
+  }
+  *scratch = g_noalloc_ptr[dev];
+  *sms = g_noalloc_sms[dev];
+  return GEMM_OK;
+}
+
+// Same launches as the handle path, with the staging area and the status word taken
+// from the static scratch (or the caller's status word) and default options.
+gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, const Plan &pl,
+                              cudaStream_t s) {
+  const gemm_plan_info_t &I = pl.info;
+  cudaError_t e;
+  switch (I.path) {
+    case GEMM_PATH_NONE: return GEMM_OK;
+    case GEMM_PATH_ZERO_FILL:
+      e = zero_fill_launch(P.C, P.ldc, P.M, P.N, P.out_dtype, s);
+      return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "zero fill launch");
+    case GEMM_PATH_FMA: {
+      FmaParams fp{P.M, P.N, P.K, P.A, P.lda, P.B, P.ldb, P.C, P.ldc, P.in_dtype, P.out_dtype,
+                   P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR};
+      e = fma_launch(fp, pl.fma_tile, s);
+      return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "fma launch");
+    }
+    default: break;
+  }
+  const size_t limit = GEMM_NOALLOC_SCRATCH_BYTES - kStaticStatusBytes;
+  if (static_cast<size_t>(I.workspace_bytes) > limit) {
+    if (log_enabled())
+      std::fprintf(stderr, "[gemm] gemm_run_noalloc: staging needs %lld bytes, limit %zu\n",
+                   static_cast<long long>(I.workspace_bytes), limit);
+    return GEMM_ERR_UNSUPPORTED;
+  }
+  char *staging = static_cast<char *>(scratch) + kStaticStatusBytes;
+  if (!status) {
+    // The static status word keeps the last call's value: clear it for this call.
+    status = static_cast<int *>(scratch);
+    e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear the static status word");
+  }
+  const int es = esize_of(P.in_dtype);
+  const void *a_ptr = pl.a.ptr;
+  int64_t a_ld = pl.a.ld;
+  const void *b_ptr = pl.b.ptr;
+  int64_t b_ld = pl.b.ld;
+  for (const OperandPlan *o : {&pl.a, &pl.b}) {
+    if (!o->staged) continue;
+    void *dst = staging + o->ws_offset;
+    e = o->transpose ? transpose_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s)
+                     : repack_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stage operand");
+    if (o == &pl.a)
+      a_ptr = dst, a_ld = o->staged_ld;
+    else
+      b_ptr = dst, b_ld = o->staged_ld;
+  }
+  const uint32_t row_elems = 128 / es;
+  CUtensorMap tmA, tmB, tmC;
+  std::memset(&tmC, 0, sizeof tmC);
+  const uint32_t a_box_outer = pl.a.mn_major ? row_elems : static_cast<uint32_t>(I.tile_m);
+  const uint32_t b_box_outer = pl.b.mn_major ? row_elems : static_cast<uint32_t>(I.tile_n);
+  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, row_elems,
+                 a_box_outer) ||
+      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
+                 b_box_outer))
+    return GEMM_ERR_CUDA;
+  if (I.tma_store) {
+    const uint32_t out_row = 128 / esize_of(P.out_dtype);
+    if (!encode_2d(&tmC, P.out_dtype, P.C, P.N, P.M, P.ldc, out_row, 32)) return GEMM_ERR_CUDA;
+  }
+  const Options defaults;
+  TcParams tp{};
+  tp.M = static_cast<int32_t>(P.M);
+  tp.N = static_cast<int32_t>(P.N);
+  tp.K = static_cast<int32_t>(P.K);
+  tp.tiles_m = static_cast<int32_t>(I.grid_m);
+  tp.tiles_n = static_cast<int32_t>(I.grid_n);
+  tp.k_blocks = static_cast<int32_t>(I.k_iters);
+  tp.group_m = static_cast<int32_t>(defaults.group_m < I.grid_m ? defaults.group_m : I.grid_m);
+  tp.idesc = make_idesc(P.in_dtype, pl.a.mn_major, pl.b.mn_major, I.tile_n, I.tile_m);
+  tp.out_dtype = P.out_dtype;
+  tp.tma_store = I.tma_store;
+  tp.C = P.C;
+  tp.ldc = P.ldc;
+  tp.status = status;
+  tp.timeout_ns = gemm_handle_s().timeout_us * 1000ull;
+  tp.debug_flags = 0;
+  e = tc_launch(pl.variant, tmA, tmB, tmC, tp, static_cast<int>(I.ctas), s);
+  return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "tcgen05 launch");
+}
+
+}  // namespace
+
+extern "C" GEMM_API gemm_status_t gemm_run_noalloc(
+    int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+    void *C, int64_t ldc, gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+    gemm_precision_t precision_mode, gemm_layout_t a_layout, gemm_layout_t b_layout,
+    int *device_status, void *cuda_stream) {
+  const Problem P{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
+                  b_layout};
+  Plan pl;
+  gemm_status_t st = check_args(P);
+  if (st != GEMM_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_DEVICE;
+  }
+  void *scratch = nullptr;
+  int sms = 0;
+  st = noalloc_setup(dev, &scratch, &sms);
+  if (st != GEMM_OK) return st;
+  st = make_plan(P, Options(), sms, &pl);
+  if (st != GEMM_OK) return st;
+  return execute_noalloc(scratch, device_status, P, pl, static_cast<cudaStream_t>(cuda_stream));
+}

@@ -185,6 +185,43 @@ GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t 
 /* Library version as "major.minor.patch". */
 GEMM_API const char *gemm_version(void);
 
+/* --------------------------------------------------- allocation-free variant */
+
+/* Size of the fixed device scratch array behind gemm_run_noalloc, in bytes. The first
+ * 256 bytes hold a status word; the rest holds staged operand copies. */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* C = A @ B like gemm_run_ex, for callers that may not allocate device memory at the
+ * point of the call -- e.g. a plugin running inside another runtime that owns every
+ * device allocation, a deployment that reserves all memory up front and forbids growth,
+ * or a host callback / real-time path where cudaMalloc (which can synchronise the
+ * device) is not allowed. The pages have no counterpart to this entry point.
+ *
+ * It takes no handle and allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine. Operands that must be staged (a base or leading dimension TMA cannot
+ * address, or an MN-major fp32 operand in tf32 mode) are copied into a file-scope device
+ * array of GEMM_NOALLOC_SCRATCH_BYTES that every GPU loading this library keeps until the
+ * process exits. A call whose staged copies would not fit returns GEMM_ERR_UNSUPPORTED
+ * before launching anything; use gemm_run_ex for it. Arguments and layouts are those of
+ * gemm_run_ex; the device is the caller's current device; default options apply.
+ *
+ * The first call on each device does a one-time set-up with that device current (it looks
+ * up the array's device address and the SM count); make that first call before any
+ * stream capture. All calls share the one array and it keeps the last call's contents:
+ * two calls that may run at the same time on the GPU (different streams, no ordering
+ * between them) race on it. Calls ordered on one stream are safe.
+ *
+ * device_status: optional caller-owned device int. A device-side bounded wait that
+ * expires stores GEMM_ERR_TIMEOUT there (if it still holds 0) and leaves C undefined.
+ * With NULL, the status word inside the scratch array is cleared and used instead, and
+ * such a failure is not reported. */
+GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A,
+                                        int64_t lda, const void *B, int64_t ldb, void *C,
+                                        int64_t ldc, gemm_dtype_t in_dtype,
+                                        gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
+                                        gemm_layout_t a_layout, gemm_layout_t b_layout,
+                                        int *device_status, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

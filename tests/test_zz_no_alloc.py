@@ -1,0 +1,80 @@
+"""gemm_run_noalloc, the entry point for callers that may not allocate device memory when
+they need a product (a plugin inside a runtime that owns every device allocation, a
+deployment that reserves all memory up front, a callback that must not synchronise the
+device the way cudaMalloc can). It stages operands in a fixed device array compiled into
+the library instead of a workspace grown with cudaMalloc.
+
+Called here through the C ABI and compared with gemm_run_ex (the handle path) on
+problems whose operands must be staged, so the fixed array is really used, on calls in
+a row that overwrite each other's staged copies."""
+import ctypes
+
+import pytest
+import torch
+
+import workloads as W
+from gpu_util import oracle_rows, rel_err, to_device, tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import dense_tiled_gemm_05_gb300 as g
+    from dense_tiled_gemm_05_gb300 import build as gbuild
+    gbuild.build()
+    return g
+
+
+def noalloc(g, a, b, out, precision, status=None):
+    al, lda = g.operand_layout(a)
+    bl, ldb = g.operand_layout(b)
+    M, K = a.shape
+    N = b.shape[1]
+    stream = torch.cuda.current_stream().cuda_stream
+    return g.lib().gemm_run_noalloc(
+        M, N, K, ctypes.c_void_p(a.data_ptr()), lda, ctypes.c_void_p(b.data_ptr()), ldb,
+        ctypes.c_void_p(out.data_ptr()), max(out.stride(0), N, 1), g._dtype_code(a.dtype),
+        g._dtype_code(out.dtype), g.PREC[precision], al, bl,
+        None if status is None else ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream))
+
+
+def test_noalloc_matches_run_ex_on_calls_in_a_row(g):
+    h = g.Gemm(0)
+    # Both need staging: fp16 rows of 1025 elements are not 16-byte multiples, and a
+    # row-major B in tf32 mode is transposed into K-major form.
+    problems = [W.ragged(1023, 1000, 1025), W.fp32_square(1000, "tf32", seed=21),
+                W.ragged(1023, 1000, 1025)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for n, p in enumerate(problems):
+        a, b = to_device(p.A), to_device(p.B)
+        plan = g.plan(a, b, out_dtype=p.out_dtype, precision=p.precision)
+        assert plan["stage_a"] or plan["stage_b"]
+        assert plan["workspace_bytes"] <= (32 << 20) - 256  # fits the fixed array
+        ref = h.matmul(a, b, out_dtype=p.out_dtype, precision=p.precision)  # gemm_run_ex
+        assert h.status() == 0
+        out = torch.full_like(ref, float("nan"))
+        rc = noalloc(g, a, b, out, p.precision, status=status if n != 1 else None)
+        assert rc == 0, g.STATUS.get(rc, rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        C64, D = oracle_rows(p)
+        assert rel_err(out, C64, D) <= tolerance(p)
+        scale = torch.from_numpy(D).to(out.device).clamp_min(1e-30)
+        assert float(((out.double() - ref.double()).abs() / scale).max()) <= tolerance(p)
+        assert torch.equal(out, ref)  # same kernels and staging: the same bits
+    h.close()
+
+
+def test_noalloc_rejects_staging_beyond_its_array(g):
+    # A row-major 4096 x 4096 fp32 B in tf32 mode needs a 64 MiB transposed copy, more
+    # than the 32 MiB array: refused before anything is launched, C untouched.
+    a = torch.zeros(64, 4096, dtype=torch.float32, device="cuda")
+    b = torch.zeros(4096, 4096, dtype=torch.float32, device="cuda")
+    out = torch.full((64, 4096), 7.0, dtype=torch.float32, device="cuda")
+    rc = noalloc(g, a, b, out, "tf32")
+    assert rc == 2  # GEMM_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
