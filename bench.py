@@ -41,8 +41,10 @@ METRIC = "GEMM TFLOP/s and % of GB300 dense tensor peak (1 GPU) vs CPU oracle"
 DATASHEET_BF16_TFLOPS = 2250.0  # dense bf16, NVIDIA GB300 (nominal)
 TF32_OVER_BF16 = 1100.0 / 2250.0  # nominal dense tf32 / bf16 ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_bf16_8192.md")
-TC_SOURCE = os.path.join(ROOT, "dense_tiled_gemm_05_gb300", "csrc", "tc_kernel.cu")
+PROFILE = os.path.join(ROOT, "profiles", "tc2_gemm_cta_pair_bf16_8192.md")
+CSRC = os.path.join(ROOT, "dense_tiled_gemm_05_gb300", "csrc")
+# sources of the kernel the default workload runs (the CTA-pair tensor-core kernel)
+TC_SOURCES = [os.path.join(CSRC, f) for f in ("tc2_kernel.cu", "tc_common.cuh", "ptx.cuh")]
 
 
 def workload(name):
@@ -89,8 +91,10 @@ def profile_traffic():
     s = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not s:
         return None
-    cur = hashlib.sha256(open(TC_SOURCE, "rb").read()).hexdigest()
-    return float(m.group(1)) if s.group(1) == cur else None
+    h = hashlib.sha256()
+    for f in TC_SOURCES:
+        h.update(open(f, "rb").read())
+    return float(m.group(1)) if s.group(1) == h.hexdigest() else None
 
 
 class ClockSampler:

@@ -35,6 +35,7 @@ struct gemm_handle_s {
   int max_ctas = 0;
   int stall_producer = 0;
   int force_staging = 0;
+  int cta_pair = 0;  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
 };
 
 namespace {
@@ -116,7 +117,7 @@ struct Problem {
 };
 
 struct Options {
-  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0;
+  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0;
 };
 
 // An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
@@ -266,8 +267,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
   pl.variant.block_n = 256;
+  // CTA pairs (256 x 256 tiles on two SMs) halve the shared-memory and L2 traffic per
+  // flop; a problem no taller than one 128-row tile keeps single-CTA tiles.
+  pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM);
   I.path = GEMM_PATH_TCGEN05;
-  I.tile_m = kTcBlockM;
+  I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
   I.tile_n = pl.variant.block_n;
   I.tile_k = 128 / es;
   I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
@@ -283,10 +287,18 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   I.tma_store = reinterpret_cast<uintptr_t>(P.C) % 16 == 0 && (P.ldc * os) % 16 == 0 &&
                 (P.N * os) % 16 == 0;
   const int64_t tiles = I.grid_m * I.grid_n;
-  int64_t ctas = sm_count > 0 ? sm_count : 1;
-  if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
-  I.ctas = tiles < ctas ? tiles : ctas;
+  if (pl.variant.pair) {
+    // One cluster of two CTAs per tile slot; the launch clamps to the clusters that fit.
+    int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
+    if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
+    I.ctas = 2 * (tiles < clusters ? tiles : clusters);
+  } else {
+    int64_t ctas = sm_count > 0 ? sm_count : 1;
+    if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
+    I.ctas = tiles < ctas ? tiles : ctas;
+  }
   I.workspace_bytes = static_cast<int64_t>(cursor);
+  I.cta_pair = pl.variant.pair ? 1 : 0;
   *out = pl;
   return GEMM_OK;
 }
@@ -359,8 +371,60 @@ Options options_of(gemm_handle_t h) {
     o.group_m = h->group_m;
     o.max_ctas = h->max_ctas;
     o.force_staging = h->force_staging;
+    o.cta_pair = h->cta_pair;
   }
   return o;
+}
+
+// Tensor maps, kernel parameters and launch of the tensor-core kernel for operands that
+// are already TMA-legal (in place or staged).
+gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
+                        const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,
+                        int group_m, int debug_flags, cudaStream_t s) {
+  const gemm_plan_info_t &I = pl.info;
+  const int es = esize_of(P.in_dtype);
+  const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
+  CUtensorMap tmA, tmB, tmC;
+  std::memset(&tmC, 0, sizeof tmC);
+  // K-major operand: box = (one 128-byte row of K) x (the CTA's rows of the tile);
+  // MN-major operand: box = (one 128-byte row of M or N) x (the stage's K rows).
+  const uint32_t cta_rows_a = kTcBlockM;
+  const uint32_t cta_rows_b = pl.variant.pair ? I.tile_n / 2 : I.tile_n;
+  const uint32_t a_box_outer = pl.a.mn_major ? row_elems : cta_rows_a;
+  const uint32_t b_box_outer = pl.b.mn_major ? row_elems : cta_rows_b;
+  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, row_elems,
+                 a_box_outer) ||
+      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
+                 b_box_outer))
+    return GEMM_ERR_CUDA;
+  if (I.tma_store) {
+    const uint32_t out_row = 128 / esize_of(P.out_dtype);
+    if (!encode_2d(&tmC, P.out_dtype, P.C, P.N, P.M, P.ldc, out_row, 32)) return GEMM_ERR_CUDA;
+  }
+  TcParams tp{};
+  tp.M = static_cast<int32_t>(P.M);
+  tp.N = static_cast<int32_t>(P.N);
+  tp.K = static_cast<int32_t>(P.K);
+  tp.tiles_m = static_cast<int32_t>(I.grid_m);
+  tp.tiles_n = static_cast<int32_t>(I.grid_n);
+  tp.k_blocks = static_cast<int32_t>(I.k_iters);
+  tp.group_m = static_cast<int32_t>(group_m < I.grid_m ? group_m : I.grid_m);
+  tp.idesc = make_idesc(P.in_dtype, pl.a.mn_major, pl.b.mn_major, I.tile_n, I.tile_m);
+  tp.out_dtype = P.out_dtype;
+  tp.tma_store = I.tma_store;
+  tp.C = P.C;
+  tp.ldc = P.ldc;
+  tp.status = status;
+  tp.timeout_ns = timeout_ns;
+  tp.debug_flags = debug_flags;
+  int64_t grid = I.ctas;
+  if (pl.variant.pair) {
+    const int64_t fit = tc2_max_active_clusters();
+    if (fit <= 0) return GEMM_ERR_CUDA;
+    if (grid / 2 > fit) grid = 2 * fit;
+  }
+  const cudaError_t e = tc_launch(pl.variant, tmA, tmB, tmC, tp, static_cast<int>(grid), s);
+  return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "tcgen05 launch");
 }
 
 gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s) {
@@ -403,40 +467,9 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
     else
       b_ptr = dst, b_ld = o->staged_ld;
   }
-  const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
-  CUtensorMap tmA, tmB, tmC;
-  std::memset(&tmC, 0, sizeof tmC);
-  // K-major operand: box = (one 128-byte row of K) x (tile rows); MN-major operand:
-  // box = (one 128-byte row of M or N) x (the stage's K rows).
-  const uint32_t a_box_outer = pl.a.mn_major ? row_elems : static_cast<uint32_t>(I.tile_m);
-  const uint32_t b_box_outer = pl.b.mn_major ? row_elems : static_cast<uint32_t>(I.tile_n);
-  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, row_elems,
-                 a_box_outer) ||
-      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
-                 b_box_outer))
-    return GEMM_ERR_CUDA;
-  if (I.tma_store) {
-    const uint32_t out_row = 128 / esize_of(P.out_dtype);
-    if (!encode_2d(&tmC, P.out_dtype, P.C, P.N, P.M, P.ldc, out_row, 32)) return GEMM_ERR_CUDA;
-  }
-  TcParams tp{};
-  tp.M = static_cast<int32_t>(P.M);
-  tp.N = static_cast<int32_t>(P.N);
-  tp.K = static_cast<int32_t>(P.K);
-  tp.tiles_m = static_cast<int32_t>(I.grid_m);
-  tp.tiles_n = static_cast<int32_t>(I.grid_n);
-  tp.k_blocks = static_cast<int32_t>(I.k_iters);
-  tp.group_m = static_cast<int32_t>(h->group_m < I.grid_m ? h->group_m : I.grid_m);
-  tp.idesc = make_idesc(P.in_dtype, pl.a.mn_major, pl.b.mn_major, I.tile_n, I.tile_m);
-  tp.out_dtype = P.out_dtype;
-  tp.tma_store = I.tma_store;
-  tp.C = P.C;
-  tp.ldc = P.ldc;
-  tp.status = h->status;
-  tp.timeout_ns = h->timeout_us * 1000ull;
-  tp.debug_flags = h->stall_producer ? kDebugStallProducer : 0;
-  e = tc_launch(pl.variant, tmA, tmB, tmC, tp, static_cast<int>(I.ctas), s);
-  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 launch");
+  st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
+                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, s);
+  if (st != GEMM_OK) return st;
   h->launches += 1;
   return GEMM_OK;
 }
@@ -525,6 +558,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
     case GEMM_OPT_FORCE_STAGING:
       if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
       h->force_staging = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_CTA_PAIR:
+      if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
+      h->cta_pair = static_cast<int>(v);
       return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
@@ -693,39 +730,9 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
     else
       b_ptr = dst, b_ld = o->staged_ld;
   }
-  const uint32_t row_elems = 128 / es;
-  CUtensorMap tmA, tmB, tmC;
-  std::memset(&tmC, 0, sizeof tmC);
-  const uint32_t a_box_outer = pl.a.mn_major ? row_elems : static_cast<uint32_t>(I.tile_m);
-  const uint32_t b_box_outer = pl.b.mn_major ? row_elems : static_cast<uint32_t>(I.tile_n);
-  if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, row_elems,
-                 a_box_outer) ||
-      !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
-                 b_box_outer))
-    return GEMM_ERR_CUDA;
-  if (I.tma_store) {
-    const uint32_t out_row = 128 / esize_of(P.out_dtype);
-    if (!encode_2d(&tmC, P.out_dtype, P.C, P.N, P.M, P.ldc, out_row, 32)) return GEMM_ERR_CUDA;
-  }
   const Options defaults;
-  TcParams tp{};
-  tp.M = static_cast<int32_t>(P.M);
-  tp.N = static_cast<int32_t>(P.N);
-  tp.K = static_cast<int32_t>(P.K);
-  tp.tiles_m = static_cast<int32_t>(I.grid_m);
-  tp.tiles_n = static_cast<int32_t>(I.grid_n);
-  tp.k_blocks = static_cast<int32_t>(I.k_iters);
-  tp.group_m = static_cast<int32_t>(defaults.group_m < I.grid_m ? defaults.group_m : I.grid_m);
-  tp.idesc = make_idesc(P.in_dtype, pl.a.mn_major, pl.b.mn_major, I.tile_n, I.tile_m);
-  tp.out_dtype = P.out_dtype;
-  tp.tma_store = I.tma_store;
-  tp.C = P.C;
-  tp.ldc = P.ldc;
-  tp.status = status;
-  tp.timeout_ns = gemm_handle_s().timeout_us * 1000ull;
-  tp.debug_flags = 0;
-  e = tc_launch(pl.variant, tmA, tmB, tmC, tp, static_cast<int>(I.ctas), s);
-  return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "tcgen05 launch");
+  return launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, status, gemm_handle_s().timeout_us * 1000ull,
+                   defaults.group_m, 0, s);
 }
 
 }  // namespace

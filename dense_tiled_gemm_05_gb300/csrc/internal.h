@@ -37,12 +37,18 @@ struct TcVariant {
   int esize;
   bool a_mn, b_mn;
   int block_n;
+  bool pair;  // CTA pair (cta_group::2): 256 x 256 tiles over two SMs
 };
 
 int tc_stages(const TcVariant &v);
 size_t tc_smem_bytes(const TcVariant &v);
 cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+// CTA-pair kernel: grid counts CTAs (twice the clusters).
+cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+// Clusters of two CTAs of the pair kernel that fit on the current device at once.
+int tc2_max_active_clusters();
 
 // fp32 fused-multiply-add tile kernel (exact fp32 mode; any input dtype/layout).
 struct FmaParams {

@@ -1,0 +1,321 @@
+// tc2_kernel.cu -- the tensor-core blocked GEMM on CTA pairs (cta_group::2, two SMs).
+//
+// Same computation and roles as tc_kernel.cu ("Chapter 13: The Blocked Matmul Kernel",
+// section 13.1: a grid of output tiles, each walking its K-chunks into an fp32 accumulator
+// initialised once; section 13.2's masks from the TMA unit's zero fill and clipped stores),
+// but each output tile is 256 x 256 and is computed by a cluster of two CTAs on two SMs:
+//   * each CTA TMA-loads its own 128 rows of A and its own 128 columns of B per K-chunk
+//     into its shared memory and signals the leader CTA's full barrier;
+//   * the leader's MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256): the
+//     hardware reads A and B halves from both CTAs' shared memory and writes rows 0-127 of
+//     the accumulator to the leader's TMEM and rows 128-255 to the peer's TMEM;
+//   * commits multicast to the barriers of both CTAs (stage free; accumulator ready);
+//   * both CTAs' epilogue warps drain their own TMEM and release the leader's TMEM-empty
+//     barrier (the peer arrives remotely).
+// Each SM therefore streams half as much B per flop as the single-CTA 128 x 256 tile, and
+// each output tile needs half the L2 traffic per flop.
+#include "tc_common.cuh"
+
+namespace gemm_gb300 {
+namespace {
+
+using namespace tc;
+
+template <int ESIZE, bool A_MN, bool B_MN>
+struct Cfg2 {
+  static constexpr int BM = kTcBlockM;             // rows per CTA (256 per pair)
+  static constexpr int BN = 256;                   // columns per pair tile
+  static constexpr int BN_HALF = BN / 2;           // B columns loaded by each CTA
+  static constexpr int BK = kRowBytes / ESIZE;     // K elements per stage
+  static constexpr int UMMA_K = 32 / ESIZE;        // K elements per tcgen05.mma
+  static constexpr int K_STEPS = BK / UMMA_K;
+  static constexpr int PANEL = kRowBytes / ESIZE;  // M/N elements per 128-byte row (MN-major)
+  static constexpr int PANEL_BYTES = BK * kRowBytes;
+  static constexpr int A_BYTES = BM * BK * ESIZE;
+  static constexpr int B_BYTES = BN_HALF * BK * ESIZE;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
+  static constexpr int STAGES = 6;
+  static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int EPI_BYTES = kEpiWarps * 2 * kStoreBufBytes;
+  static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int ESIZE, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using G = Cfg2<ESIZE, A_MN, B_MN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::BAR_OFFSET);
+  uint64_t *empty = full + G::STAGES;
+  uint64_t *tmem_full = empty + G::STAGES;
+  uint64_t *tmem_empty = tmem_full + 2;
+  uint64_t *drain = tmem_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::STAGES; ++s) {
+      mbar_init(&full[s], 1);   // the leader's arrive.expect_tx (bytes of both CTAs)
+      mbar_init(&empty[s], 1);  // the leader's multicast commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);               // the leader's multicast commit
+      mbar_init(&tmem_empty[b], 2 * kEpiWarps);  // one arrive per epilogue warp, both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (p.tma_store) prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), G::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised; TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int cluster_id = blockIdx.x / 2;
+  const int num_clusters = gridDim.x / 2;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+        int pm, pn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+        const int m0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM;
+        const int n0 = pn * G::BN + static_cast<int>(rank) * G::BN_HALF;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
+          const uint32_t a_dst = smem_u32(smem + stage * G::STAGE_BYTES);
+          const uint32_t b_dst = a_dst + G::A_BYTES;
+          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);  // the leader's barrier
+          const int k0 = kb * G::BK;
+          if (A_MN) {
+#pragma unroll
+            for (int q = 0; q < G::BM / G::PANEL; ++q)
+              tma_load_2d_pair(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0);
+          } else {
+            tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int q = 0; q < G::BN_HALF / G::PANEL; ++q)
+              tma_load_2d_pair(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0);
+          } else {
+            tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
+          }
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+        if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, wd)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * G::BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], phase, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
+          const uint32_t b_base = a_base + G::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < G::K_STEPS; ++kk) {
+            const uint64_t ad =
+                A_MN ? sdesc_sw128(a_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
+                     : sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd =
+                B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
+                     : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            const uint32_t accumulate = (kb | kk) != 0;
+            if (ESIZE == 2)
+              mma_f16_pair(d_tmem, ad, bd, p.idesc, accumulate);
+            else
+              mma_tf32_pair(d_tmem, ad, bd, p.idesc, accumulate);
+          }
+          mma_commit_pair_multicast(&empty[stage], 0x3);  // stage free in both CTAs
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_multicast(&tmem_full[acc], 0x3);  // accumulator ready in both CTAs
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      mma_commit_pair(drain);  // every MMA issued above completes before TMEM is released
+      drain_wait(drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    uint8_t *bufs = smem + G::EPI_OFFSET + (warp - 2) * 2 * kStoreBufBytes;
+    int buf = 0;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+      bool ok = mbar_wait_cluster(&tmem_full[acc], acc_phase, wd);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      int pm, pn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+      const int row0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM + quarter * 32;
+      const int n0 = pn * G::BN;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * G::BN;
+      if (p.tma_store) {
+        if (p.out_dtype == GEMM_BF16)
+          epilogue_tma<G::BN, GEMM_BF16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+        else if (p.out_dtype == GEMM_F16)
+          epilogue_tma<G::BN, GEMM_F16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+        else
+          epilogue_tma<G::BN, GEMM_F32>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+      } else {
+        if (p.out_dtype == GEMM_BF16)
+          epilogue_direct<G::BN, GEMM_BF16>(p, t_row, row0 + lane, n0);
+        else if (p.out_dtype == GEMM_F16)
+          epilogue_direct<G::BN, GEMM_F16>(p, t_row, row0 + lane, n0);
+        else
+          epilogue_direct<G::BN, GEMM_F32>(p, t_row, row0 + lane, n0);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // After an abort, give TMA copies already issued time to land before the CTA leaves
+    // (their barrier may live in the other CTA, so they cannot be waited on here).
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000) __nanosleep(1000);
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();  // both CTAs done: no more remote arrivals, all MMAs drained
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
+  }
+}
+
+template <int ESIZE, bool A_MN, bool B_MN>
+cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                        const TcParams &p, int grid, cudaStream_t s) {
+  using G = Cfg2<ESIZE, A_MN, B_MN>;
+  auto kernel = tc2_gemm_kernel<ESIZE, A_MN, B_MN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, p);
+}
+
+template <int ESIZE>
+cudaError_t launch_pair_majors(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                               const CUtensorMap &tmC, const TcParams &p, int grid,
+                               cudaStream_t s) {
+  if (!v.a_mn && !v.b_mn) return launch_pair<ESIZE, false, false>(tmA, tmB, tmC, p, grid, s);
+  if (!v.a_mn && v.b_mn) return launch_pair<ESIZE, false, true>(tmA, tmB, tmC, p, grid, s);
+  if (v.a_mn && !v.b_mn) return launch_pair<ESIZE, true, false>(tmA, tmB, tmC, p, grid, s);
+  return launch_pair<ESIZE, true, true>(tmA, tmB, tmC, p, grid, s);
+}
+
+}  // namespace
+
+int tc2_max_active_clusters() {
+  static int cached[64];  // per device; 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cached[dev] > 0) return cached[dev];
+  using G = Cfg2<2, false, false>;
+  auto kernel = tc2_gemm_kernel<2, false, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
+  if (v.esize == 2) return launch_pair_majors<2>(v, tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 4) return launch_pair_majors<4>(v, tmA, tmB, tmC, p, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gemm_gb300

@@ -20,21 +20,12 @@
 // overlaps the main loop of tile t+1. Tiles are visited in grouped raster order
 // (GROUP_M tile-rows at a time) so that consecutive tiles on the machine share A and B
 // panels in L2.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include <type_traits>
-
-#include "internal.h"
-#include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace gemm_gb300 {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
-constexpr int kRowBytes = 128;                   // one 128-byte swizzle row
-constexpr int kStoreBufBytes = 32 * kRowBytes;   // one epilogue staging box: 32 rows x 128 B
+using namespace tc;
 
 template <int ESIZE, bool A_MN, bool B_MN, int BN>
 struct Cfg {
@@ -58,121 +49,6 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
 };
-
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
-                                            int &pm, int &pn) {
-  const int per_group = group_m * tiles_n;
-  const int g = tile / per_group;
-  const int first_m = g * group_m;
-  const int gsize = min(tiles_m - first_m, group_m);
-  const int r = tile - g * per_group;
-  pm = first_m + r % gsize;
-  pn = r / gsize;
-}
-
-// Time-bounded wait used only while tearing down after an abort: it ignores the abort
-// flag (the point is to let in-flight copies and MMAs land) and records nothing.
-__device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(a, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return;
-  }
-}
-
-__device__ __forceinline__ uint32_t pack2_bf16(uint32_t a, uint32_t b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(a), __uint_as_float(b));
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ uint32_t pack2_f16(uint32_t a, uint32_t b) {
-  __half2 h = __floats2half2_rn(__uint_as_float(a), __uint_as_float(b));
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
-template <int OUT>
-__device__ __forceinline__ uint32_t pack2(uint32_t a, uint32_t b) {
-  return OUT == GEMM_BF16 ? pack2_bf16(a, b) : pack2_f16(a, b);
-}
-
-// Epilogue, TMA-store form: one 32-row slab of the tile per warp; each 128-byte-wide
-// column block is converted, written to a 128B-swizzled staging box and stored by TMA
-// (which clips rows >= M and columns >= N). Two staging boxes per warp alternate.
-template <int BN, int OUT>
-__device__ __forceinline__ void epilogue_tma(const CUtensorMap *tmC, uint32_t t_row, uint8_t *bufs,
-                                             int &buf, int lane, int row0, int n0, int M,
-                                             int N) {
-  constexpr int OUT_COLS = OUT == GEMM_F32 ? 32 : 64;  // columns per 128-byte staging row
-  const bool rows_in = row0 < M;
-#pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += OUT_COLS) {
-    uint32_t r0[32], r1[32];
-    tmem_ld_32x32b_x32(t_row + c0, r0);
-    if (OUT_COLS == 64) tmem_ld_32x32b_x32(t_row + c0 + 32, r1);
-    tmem_wait_ld();
-    if (!rows_in || n0 + c0 >= N) continue;  // warp-uniform: nothing of this box is in C
-    uint8_t *sb = bufs + buf * kStoreBufBytes;
-    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `sb` has read it
-    __syncwarp();
-    const uint32_t row_addr = smem_u32(sb) + lane * kRowBytes;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      uint32_t w0, w1, w2, w3;
-      if (OUT == GEMM_F32) {
-        w0 = r0[ch * 4 + 0], w1 = r0[ch * 4 + 1], w2 = r0[ch * 4 + 2], w3 = r0[ch * 4 + 3];
-      } else {
-        const int c = (ch & 3) * 8;
-        const uint32_t *r = ch < 4 ? r0 : r1;
-        w0 = pack2<OUT>(r[c + 0], r[c + 1]);
-        w1 = pack2<OUT>(r[c + 2], r[c + 3]);
-        w2 = pack2<OUT>(r[c + 4], r[c + 5]);
-        w3 = pack2<OUT>(r[c + 6], r[c + 7]);
-      }
-      const uint32_t dst = row_addr + ((ch ^ (lane & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w0), "r"(w1),
-                   "r"(w2), "r"(w3)
-                   : "memory");
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tmC, smem_u32(sb), n0 + c0, row0);
-      bulk_commit_group();
-    }
-    buf ^= 1;
-  }
-}
-
-// Epilogue, direct form for a C that TMA cannot address (misaligned base or ldc): each
-// lane owns one row and writes its in-range columns with plain stores.
-template <int BN, int OUT>
-__device__ __forceinline__ void epilogue_direct(const TcParams &p, uint32_t t_row, int row, int n0) {
-  using T = typename std::conditional<OUT == GEMM_F32, float,
-            typename std::conditional<OUT == GEMM_BF16, __nv_bfloat16, __half>::type>::type;
-#pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(t_row + c0, r);
-    tmem_wait_ld();
-    const int col = n0 + c0;
-    if (row >= p.M || col >= p.N) continue;
-    T *dst = reinterpret_cast<T *>(p.C) + static_cast<int64_t>(row) * p.ldc + col;
-    const int n = min(32, p.N - col);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < n) {
-        const float v = __uint_as_float(r[j]);
-        if (OUT == GEMM_F32) {
-          reinterpret_cast<float *>(dst)[j] = v;
-        } else if (OUT == GEMM_BF16) {
-          reinterpret_cast<__nv_bfloat16 *>(dst)[j] = __float2bfloat16_rn(v);
-        } else {
-          reinterpret_cast<__half *>(dst)[j] = __float2half_rn(v);
-        }
-      }
-    }
-  }
-}
 
 template <int ESIZE, bool A_MN, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -389,7 +265,7 @@ cudaError_t launch_majors(const TcVariant &v, const CUtensorMap &tmA, const CUte
 
 }  // namespace
 
-int tc_stages(const TcVariant &v) { return v.block_n >= 256 ? 4 : 6; }
+int tc_stages(const TcVariant &v) { return v.pair ? 6 : v.block_n >= 256 ? 4 : 6; }
 
 size_t tc_smem_bytes(const TcVariant &v) {
   if (v.block_n == 256) return Cfg<2, false, false, 256>::SMEM_BYTES;
@@ -398,6 +274,7 @@ size_t tc_smem_bytes(const TcVariant &v) {
 
 cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
+  if (v.pair) return tc2_launch(v, tmA, tmB, tmC, p, grid, s);
   if (v.esize == 2 && v.block_n == 256) return launch_majors<2, 256>(v, tmA, tmB, tmC, p, grid, s);
   if (v.esize == 4 && v.block_n == 256) return launch_majors<4, 256>(v, tmA, tmB, tmC, p, grid, s);
   if (v.esize == 2 && v.block_n == 128) return launch_majors<2, 128>(v, tmA, tmB, tmC, p, grid, s);

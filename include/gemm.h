@@ -141,7 +141,9 @@ typedef enum {
   GEMM_OPT_FAULT_STALL_PRODUCER = 4, /* test hook: the tensor-core kernel's loader issues
                                         nothing, so the consumers' bounded waits expire and the
                                         kernel reports GEMM_ERR_TIMEOUT; 0 = off */
-  GEMM_OPT_FORCE_STAGING = 5    /* 1 = stage A and B through the workspace even when aligned */
+  GEMM_OPT_FORCE_STAGING = 5,   /* 1 = stage A and B through the workspace even when aligned */
+  GEMM_OPT_CTA_PAIR = 6         /* tensor-core tiles: 0 auto, 1 single-CTA 128 x 256,
+                                   2 CTA-pair 256 x 256 (cta_group::2 on two SMs) */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
@@ -168,8 +170,10 @@ typedef struct {
   int32_t stage_a, stage_b; /* 1 if the operand is copied to an aligned workspace first */
   int32_t a_mn_major, b_mn_major; /* operand read M/N-major (1) or K-major (0) */
   int32_t tma_store;      /* 1 if the epilogue writes C with TMA stores */
-  int64_t ctas;           /* CTAs launched (persistent schedule) */
+  int64_t ctas;           /* CTAs launched (persistent schedule; pairs count twice) */
   int64_t workspace_bytes; /* workspace the call needs */
+  int32_t cta_pair;       /* 1 if tiles run on CTA pairs (two SMs per tile) */
+  int32_t reserved;
 } gemm_plan_info_t;
 
 /* Host-only: the plan gemm_run_ex would use for these arguments on a GPU with

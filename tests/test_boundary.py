@@ -75,12 +75,16 @@ def test_plan_small_exact_uses_pages_tiles():
 def test_plan_bf16_square_is_tcgen05_k_major():
     p = g.plan(t((4096, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
                sm_count=148)
-    assert p["path"] == "tcgen05"
-    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 256, 64)
-    assert (p["grid_m"], p["grid_n"], p["k_iters"]) == (32, 16, 64)
+    assert p["path"] == "tcgen05" and p["cta_pair"] == 1
+    assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (256, 256, 64)
+    assert (p["grid_m"], p["grid_n"], p["k_iters"]) == (16, 16, 64)
     assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
     assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["tma_store"] == 1
-    assert p["ctas"] == 148 and p["workspace_bytes"] == 0
+    assert p["ctas"] == 148 and p["workspace_bytes"] == 0 and p["stages"] == 6
+    # One 128-row tile of M: single-CTA tiles.
+    p = g.plan(t((128, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
+               sm_count=148)
+    assert p["cta_pair"] == 0 and (p["tile_m"], p["grid_m"], p["ctas"]) == (128, 1, 16)
 
 
 def test_plan_row_major_b_is_mn_major():

@@ -21,10 +21,12 @@ def g():
     return g
 
 
-def test_bounded_wait_expires_and_context_stays_usable(g):
+@pytest.mark.parametrize("cta_pair", [1, 2])
+def test_bounded_wait_expires_and_context_stays_usable(g, cta_pair):
     p = W.bf16_square(512)
     a, b = to_device(p.A), to_device(p.B)
     h = g.Gemm(0)
+    h.set_option("cta_pair", cta_pair)
     h.set_option("wait_timeout_us", 20000)  # 20 ms
     h.set_option("fault_stall_producer", 1)
     h.matmul(a, b)  # launches; the failure is found on the device

@@ -125,14 +125,24 @@ INT_SHAPES = [(1, 1, 1), (128, 256, 64), (129, 257, 65), (300, 520, 1025), (777,
               (64, 600, 8), (1000, 1000, 17)]
 
 
+@pytest.fixture(scope="module", params=[1, 2], ids=["single_cta", "cta_pair"])
+def h_tiles(request, h):
+    """A handle forced to single-CTA 128 x 256 tiles or to CTA-pair 256 x 256 tiles."""
+    import dense_tiled_gemm_05_gb300 as g
+    hh = g.Gemm(0)
+    hh.set_option("cta_pair", request.param)
+    yield hh
+    hh.close()
+
+
 @pytest.mark.parametrize("dtype,precision", [("bf16", "default"), ("f16", "default"),
                                              ("f32", "tf32"), ("f32", "exact")])
 @pytest.mark.parametrize("a_layout,b_layout", list(itertools.product(["row", "col"], repeat=2)))
-def test_integer_inputs_bit_exact(h, dtype, precision, a_layout, b_layout):
+def test_integer_inputs_bit_exact(h_tiles, dtype, precision, a_layout, b_layout):
     for n, (M, N, K) in enumerate(INT_SHAPES):
         p = W.integer_problem(M, N, K, dtype, seed=100 + n, a_layout=a_layout,
                               b_layout=b_layout, precision=precision, ld_pad=n % 3)
-        c = run_gpu(h, p)
+        c = run_gpu(h_tiles, p)
         ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
         assert torch.equal(c.cpu().to(torch.int64), ref), (M, N, K)
         assert torch.equal(c.cpu(), ref.to(torch.float32))
@@ -221,10 +231,12 @@ def test_schedule_options_do_not_change_bits(h):
     assert rel_err(base, C64, D) <= 1e-2
 
 
-def test_mid_size_full_compare_many_tiles_per_cta(h):
+@pytest.mark.parametrize("cta_pair,max_ctas", [(1, 7), (2, 6)])
+def test_mid_size_full_compare_many_tiles_per_cta(h, cta_pair, max_ctas):
     import dense_tiled_gemm_05_gb300 as g
     h2 = g.Gemm(0)
-    h2.set_option("max_ctas", 7)  # about 20 tiles per CTA: both TMEM buffers, many phases
+    h2.set_option("cta_pair", cta_pair)
+    h2.set_option("max_ctas", max_ctas)  # many tiles per CTA: both TMEM buffers, many phases
     for p in (W.integer_problem(2048, 1100, 1000, "bf16", seed=9, b_layout="col"),
               W.integer_problem(1500, 1024, 700, "f32", seed=10, precision="tf32")):
         c = run_gpu(h2, p)
