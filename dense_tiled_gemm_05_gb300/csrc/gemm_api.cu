@@ -36,6 +36,7 @@ struct gemm_handle_s {
   int stall_producer = 0;
   int force_staging = 0;
   int cta_pair = 0;  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
+  int block_n = 0;   // 0 auto, else 128 or 256
 };
 
 namespace {
@@ -117,7 +118,7 @@ struct Problem {
 };
 
 struct Options {
-  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0;
+  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
 };
 
 // An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
@@ -221,6 +222,23 @@ OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, 
   return o;
 }
 
+// Tile width by a wave-quantisation cost model: a persistent grid runs
+// ceil(tiles / slots) rounds, each as long as one tile. A 128-wide tile has half the
+// flops of a 256-wide one but, measured on GB300, takes about 0.75 of its time (every MMA
+// re-reads its 128 x 16 slice of A from shared memory, so narrow MMAs are starved of
+// shared-memory bandwidth); it wins only when it fills the machine much better, e.g.
+// when N itself is at most 128.
+int pick_block_n(int64_t M, int64_t N, bool pair, int sm_count) {
+  const int64_t rows = pair ? 2 * kTcBlockM : kTcBlockM;
+  const int64_t slots = pair ? (sm_count > 1 ? sm_count / 2 : 1) : (sm_count > 0 ? sm_count : 1);
+  const int64_t tiles_m = (M + rows - 1) / rows;
+  auto cost = [&](int64_t bn, double per_column) {
+    const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+    return static_cast<double>((tiles + slots - 1) / slots) * static_cast<double>(bn) * per_column;
+  };
+  return cost(128, 1.5) < cost(256, 1.0) ? 128 : 256;
+}
+
 gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan *out) {
   gemm_status_t st = check_args(P);
   if (st != GEMM_OK) return st;
@@ -266,10 +284,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   pl.variant.esize = es;
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
-  pl.variant.block_n = 256;
-  // CTA pairs (256 x 256 tiles on two SMs) halve the shared-memory and L2 traffic per
+  // CTA pairs (256-row tiles on two SMs) halve the shared-memory and L2 traffic per
   // flop; a problem no taller than one 128-row tile keeps single-CTA tiles.
   pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM);
+  pl.variant.block_n = opt.block_n ? opt.block_n
+                                   : pick_block_n(P.M, P.N, pl.variant.pair, sm_count);
   I.path = GEMM_PATH_TCGEN05;
   I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
   I.tile_n = pl.variant.block_n;
@@ -372,6 +391,7 @@ Options options_of(gemm_handle_t h) {
     o.max_ctas = h->max_ctas;
     o.force_staging = h->force_staging;
     o.cta_pair = h->cta_pair;
+    o.block_n = h->block_n;
   }
   return o;
 }
@@ -562,6 +582,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
     case GEMM_OPT_CTA_PAIR:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_BLOCK_N:
+      if (v != 0 && v != 128 && v != 256) return GEMM_ERR_INVALID_ARG;
+      h->block_n = static_cast<int>(v);
       return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;

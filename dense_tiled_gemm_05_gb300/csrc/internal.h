@@ -41,7 +41,6 @@ struct TcVariant {
 };
 
 int tc_stages(const TcVariant &v);
-size_t tc_smem_bytes(const TcVariant &v);
 cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
 // CTA-pair kernel: grid counts CTAs (twice the clusters).

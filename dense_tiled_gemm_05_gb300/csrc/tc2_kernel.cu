@@ -21,10 +21,10 @@ namespace {
 
 using namespace tc;
 
-template <int ESIZE, bool A_MN, bool B_MN>
+template <int ESIZE, bool A_MN, bool B_MN, int BN_>
 struct Cfg2 {
   static constexpr int BM = kTcBlockM;             // rows per CTA (256 per pair)
-  static constexpr int BN = 256;                   // columns per pair tile
+  static constexpr int BN = BN_;                   // columns per pair tile (256 or 128)
   static constexpr int BN_HALF = BN / 2;           // B columns loaded by each CTA
   static constexpr int BK = kRowBytes / ESIZE;     // K elements per stage
   static constexpr int UMMA_K = 32 / ESIZE;        // K elements per tcgen05.mma
@@ -34,7 +34,7 @@ struct Cfg2 {
   static constexpr int A_BYTES = BM * BK * ESIZE;
   static constexpr int B_BYTES = BN_HALF * BK * ESIZE;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = BN >= 256 ? 6 : 8;
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * 2 * kStoreBufBytes;
   static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
@@ -45,12 +45,12 @@ struct Cfg2 {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int ESIZE, bool A_MN, bool B_MN>
+template <int ESIZE, bool A_MN, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using G = Cfg2<ESIZE, A_MN, B_MN>;
+  using G = Cfg2<ESIZE, A_MN, B_MN, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -241,11 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int ESIZE, bool A_MN, bool B_MN>
+template <int ESIZE, bool A_MN, bool B_MN, int BN>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TcParams &p, int grid, cudaStream_t s) {
-  using G = Cfg2<ESIZE, A_MN, B_MN>;
-  auto kernel = tc2_gemm_kernel<ESIZE, A_MN, B_MN>;
+  using G = Cfg2<ESIZE, A_MN, B_MN, BN>;
+  auto kernel = tc2_gemm_kernel<ESIZE, A_MN, B_MN, BN>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -264,14 +264,14 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, p);
 }
 
-template <int ESIZE>
+template <int ESIZE, int BN>
 cudaError_t launch_pair_majors(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                                const CUtensorMap &tmC, const TcParams &p, int grid,
                                cudaStream_t s) {
-  if (!v.a_mn && !v.b_mn) return launch_pair<ESIZE, false, false>(tmA, tmB, tmC, p, grid, s);
-  if (!v.a_mn && v.b_mn) return launch_pair<ESIZE, false, true>(tmA, tmB, tmC, p, grid, s);
-  if (v.a_mn && !v.b_mn) return launch_pair<ESIZE, true, false>(tmA, tmB, tmC, p, grid, s);
-  return launch_pair<ESIZE, true, true>(tmA, tmB, tmC, p, grid, s);
+  if (!v.a_mn && !v.b_mn) return launch_pair<ESIZE, false, false, BN>(tmA, tmB, tmC, p, grid, s);
+  if (!v.a_mn && v.b_mn) return launch_pair<ESIZE, false, true, BN>(tmA, tmB, tmC, p, grid, s);
+  if (v.a_mn && !v.b_mn) return launch_pair<ESIZE, true, false, BN>(tmA, tmB, tmC, p, grid, s);
+  return launch_pair<ESIZE, true, true, BN>(tmA, tmB, tmC, p, grid, s);
 }
 
 }  // namespace
@@ -284,8 +284,8 @@ int tc2_max_active_clusters() {
     return 0;
   }
   if (cached[dev] > 0) return cached[dev];
-  using G = Cfg2<2, false, false>;
-  auto kernel = tc2_gemm_kernel<2, false, false>;
+  using G = Cfg2<2, false, false, 256>;
+  auto kernel = tc2_gemm_kernel<2, false, false, 256>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -313,8 +313,13 @@ int tc2_max_active_clusters() {
 
 cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
-  if (v.esize == 2) return launch_pair_majors<2>(v, tmA, tmB, tmC, p, grid, s);
-  if (v.esize == 4) return launch_pair_majors<4>(v, tmA, tmB, tmC, p, grid, s);
+  // tf32 operands are always K-major (MN-major fp32 operands are staged transposed).
+  if (v.esize == 2 && v.block_n == 256) return launch_pair_majors<2, 256>(v, tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 2 && v.block_n == 128) return launch_pair_majors<2, 128>(v, tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 4 && !v.a_mn && !v.b_mn) {
+    if (v.block_n == 256) return launch_pair<4, false, false, 256>(tmA, tmB, tmC, p, grid, s);
+    if (v.block_n == 128) return launch_pair<4, false, false, 128>(tmA, tmB, tmC, p, grid, s);
+  }
   return cudaErrorInvalidValue;
 }
 

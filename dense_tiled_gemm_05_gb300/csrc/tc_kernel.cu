@@ -265,20 +265,20 @@ cudaError_t launch_majors(const TcVariant &v, const CUtensorMap &tmA, const CUte
 
 }  // namespace
 
-int tc_stages(const TcVariant &v) { return v.pair ? 6 : v.block_n >= 256 ? 4 : 6; }
-
-size_t tc_smem_bytes(const TcVariant &v) {
-  if (v.block_n == 256) return Cfg<2, false, false, 256>::SMEM_BYTES;
-  return Cfg<2, false, false, 128>::SMEM_BYTES;
+int tc_stages(const TcVariant &v) {
+  if (v.pair) return v.block_n >= 256 ? 6 : 8;
+  return v.block_n >= 256 ? 4 : 6;
 }
 
 cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
   if (v.pair) return tc2_launch(v, tmA, tmB, tmC, p, grid, s);
   if (v.esize == 2 && v.block_n == 256) return launch_majors<2, 256>(v, tmA, tmB, tmC, p, grid, s);
-  if (v.esize == 4 && v.block_n == 256) return launch_majors<4, 256>(v, tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 4 && v.block_n == 256 && !v.a_mn && !v.b_mn)
+    return launch_one<4, false, false, 256>(tmA, tmB, tmC, p, grid, s);
   if (v.esize == 2 && v.block_n == 128) return launch_majors<2, 128>(v, tmA, tmB, tmC, p, grid, s);
-  if (v.esize == 4 && v.block_n == 128) return launch_majors<4, 128>(v, tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 4 && v.block_n == 128 && !v.a_mn && !v.b_mn)
+    return launch_one<4, false, false, 128>(tmA, tmB, tmC, p, grid, s);
   return cudaErrorInvalidValue;
 }
 

@@ -142,8 +142,9 @@ typedef enum {
                                         nothing, so the consumers' bounded waits expire and the
                                         kernel reports GEMM_ERR_TIMEOUT; 0 = off */
   GEMM_OPT_FORCE_STAGING = 5,   /* 1 = stage A and B through the workspace even when aligned */
-  GEMM_OPT_CTA_PAIR = 6         /* tensor-core tiles: 0 auto, 1 single-CTA 128 x 256,
-                                   2 CTA-pair 256 x 256 (cta_group::2 on two SMs) */
+  GEMM_OPT_CTA_PAIR = 6,        /* tensor-core tiles: 0 auto, 1 single-CTA (128 rows),
+                                   2 CTA-pair (256 rows, cta_group::2 on two SMs) */
+  GEMM_OPT_BLOCK_N = 7          /* tensor-core tile width: 0 auto, 128 or 256 */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */

@@ -81,10 +81,17 @@ def test_plan_bf16_square_is_tcgen05_k_major():
     assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
     assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["tma_store"] == 1
     assert p["ctas"] == 148 and p["workspace_bytes"] == 0 and p["stages"] == 6
+    p = g.plan(t((8192, 8192), torch.bfloat16), t((8192, 8192), torch.bfloat16, "col"),
+               sm_count=148)
+    assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 256, 32, 32)
+    p = g.plan(t((16384, 8192), torch.bfloat16), t((8192, 128), torch.bfloat16, "col"),
+               sm_count=148)
+    assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 128, 64, 1)
     # One 128-row tile of M: single-CTA tiles.
     p = g.plan(t((128, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
                sm_count=148)
-    assert p["cta_pair"] == 0 and (p["tile_m"], p["grid_m"], p["ctas"]) == (128, 1, 16)
+    assert p["cta_pair"] == 0 and (p["tile_m"], p["tile_n"], p["grid_m"]) == (128, 256, 1)
+    assert p["ctas"] == 16
 
 
 def test_plan_row_major_b_is_mn_major():

@@ -125,12 +125,15 @@ INT_SHAPES = [(1, 1, 1), (128, 256, 64), (129, 257, 65), (300, 520, 1025), (777,
               (64, 600, 8), (1000, 1000, 17)]
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["single_cta", "cta_pair"])
+@pytest.fixture(scope="module", params=[(1, 256), (1, 128), (2, 256), (2, 128)],
+                ids=["cta128x256", "cta128x128", "pair256x256", "pair256x128"])
 def h_tiles(request, h):
-    """A handle forced to single-CTA 128 x 256 tiles or to CTA-pair 256 x 256 tiles."""
+    """A handle forced to one tile kind: single-CTA (128 rows) or CTA-pair (256 rows),
+    128 or 256 columns wide."""
     import dense_tiled_gemm_05_gb300 as g
     hh = g.Gemm(0)
-    hh.set_option("cta_pair", request.param)
+    hh.set_option("cta_pair", request.param[0])
+    hh.set_option("block_n", request.param[1])
     yield hh
     hh.close()
 
