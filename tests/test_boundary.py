@@ -90,8 +90,9 @@ def test_plan_bf16_square_is_tcgen05_k_major():
     # One 128-row tile of M: single-CTA tiles.
     p = g.plan(t((128, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
                sm_count=148)
-    assert p["cta_pair"] == 0 and (p["tile_m"], p["tile_n"], p["grid_m"]) == (128, 256, 1)
-    assert p["ctas"] == 16
+    # Fewer tiles than SMs: 32 tiles of 128 x 128 finish sooner than 16 of 128 x 256.
+    assert p["cta_pair"] == 0 and (p["tile_m"], p["tile_n"], p["grid_m"]) == (128, 128, 1)
+    assert p["ctas"] == 32
 
 
 def test_plan_row_major_b_is_mn_major():
