@@ -124,12 +124,15 @@ struct Options {
 // An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
 // elements with leading dimension ld (in elements). It is either read in place or staged
 // into the workspace first: copied when TMA cannot address it (misaligned base or
-// leading dimension), or transposed into K-major form when it is an MN-major tf32
-// operand (the tf32 tensor-core instruction reads K-major operands only).
+// leading dimension), transposed into K-major form when it is an MN-major tf32 operand
+// (the tf32 tensor-core instruction reads K-major operands only), or split into tf32
+// hi/lo parts (exact-fp32 mode; always K-major, 3K columns).
 struct OperandPlan {
   const void *ptr;          // caller's operand
   int64_t ld, outer, inner; // caller's storage: outer lines of inner elements
-  bool staged, transpose;
+  bool staged, transpose, split3;
+  bool is_b, k_contig;      // which operand; whether its storage is K-contiguous
+  int64_t rows, k;          // logical rows (M or N) and K, for the split
   int64_t staged_ld;
   size_t ws_offset, ws_bytes;
   // as read by the kernel (after staging)
@@ -195,7 +198,8 @@ bool tma_legal(const void *p, int64_t ld, int64_t outer, int es) {
 }
 
 OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout,
-                         bool k_is_rows_dim, int es, bool force_stage, size_t *ws_cursor) {
+                         bool k_is_rows_dim, int es, bool force_stage, bool split3,
+                         size_t *ws_cursor) {
   OperandPlan o{};
   o.ptr = p;
   o.ld = ld;
@@ -203,13 +207,22 @@ OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, 
   o.inner = layout == GEMM_ROW_MAJOR ? cols : rows;
   // The operand is K-major when K is its contiguous axis.
   const bool k_inner = k_is_rows_dim ? layout == GEMM_COL_MAJOR : layout == GEMM_ROW_MAJOR;
+  o.is_b = k_is_rows_dim;
+  o.k_contig = k_inner;
+  o.rows = k_is_rows_dim ? cols : rows;
+  o.k = k_is_rows_dim ? rows : cols;
   o.mn_major = !k_inner;
   o.k_outer = o.outer;
   o.k_inner = o.inner;
-  o.transpose = o.mn_major && es == 4;
-  o.staged = o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
+  o.split3 = split3;
+  o.transpose = !split3 && o.mn_major && es == 4;
+  o.staged = split3 || o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
   if (o.staged) {
-    if (o.transpose) {
+    if (split3) {
+      o.k_outer = o.rows;
+      o.k_inner = 3 * o.k;
+      o.mn_major = false;
+    } else if (o.transpose) {
       o.k_outer = o.inner;
       o.k_inner = o.outer;
       o.mn_major = false;
@@ -255,13 +268,14 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
     *out = pl;
     return GEMM_OK;
   }
+  // Exact fp32 runs on the tensor cores as three tf32 products of split operands, except
+  // for tiny problems (the pages' 8 x 8 example and smaller), which take the fp32 FMA
+  // kernel with 4 x 4 x 4 tiles; GEMM_OPT_FORCE_PATH chooses either explicitly.
   const bool exact = P.in_dtype == GEMM_F32 && P.precision != GEMM_PREC_TF32;
-  bool use_fma = exact;
+  bool use_fma = exact && P.M * P.N <= 256;
   if (opt.force_path == 2) use_fma = true;
-  if (opt.force_path == 1) {
-    if (exact) return GEMM_ERR_UNSUPPORTED;  // the tensor cores have no exact-fp32 mode
-    use_fma = false;
-  }
+  if (opt.force_path == 1) use_fma = false;
+  const bool split = exact && !use_fma;
   if (use_fma) {
     pl.fma_tile = (P.M * P.N <= 256) ? 4 : 128;
     int bm, bn, bk;
@@ -279,8 +293,10 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   const int es = esize_of(P.in_dtype);
   const int os = esize_of(P.out_dtype);
   size_t cursor = 0;
-  pl.a = plan_operand(P.A, P.M, P.K, P.lda, P.a_layout, false, es, opt.force_staging != 0, &cursor);
-  pl.b = plan_operand(P.B, P.K, P.N, P.ldb, P.b_layout, true, es, opt.force_staging != 0, &cursor);
+  pl.a = plan_operand(P.A, P.M, P.K, P.lda, P.a_layout, false, es, opt.force_staging != 0, split,
+                      &cursor);
+  pl.b = plan_operand(P.B, P.K, P.N, P.ldb, P.b_layout, true, es, opt.force_staging != 0, split,
+                      &cursor);
   pl.variant.esize = es;
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
@@ -289,13 +305,19 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM);
   pl.variant.block_n = opt.block_n ? opt.block_n
                                    : pick_block_n(P.M, P.N, pl.variant.pair, sm_count);
-  I.path = GEMM_PATH_TCGEN05;
+  if (split) {  // the exact-fp32 kernel has one shape: CTA pairs, 256 x 256 tiles
+    pl.variant.exact = true;
+    pl.variant.pair = true;
+    pl.variant.block_n = 256;
+  }
+  I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : GEMM_PATH_TCGEN05;
   I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
   I.tile_n = pl.variant.block_n;
   I.tile_k = 128 / es;
   I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
   I.grid_n = (P.N + I.tile_n - 1) / I.tile_n;
-  I.k_iters = (P.K + I.tile_k - 1) / I.tile_k;
+  const int64_t k_total = split ? 3 * P.K : P.K;  // split operands concatenate 3 products
+  I.k_iters = (k_total + I.tile_k - 1) / I.tile_k;
   if (I.grid_m * I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   I.stages = tc_stages(pl.variant);
   I.stage_a = pl.a.staged, I.stage_b = pl.b.staged;
@@ -396,6 +418,14 @@ Options options_of(gemm_handle_t h) {
   return o;
 }
 
+cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t s) {
+  if (o.split3)
+    return split3_launch(static_cast<const float *>(o.ptr), o.ld, o.k_contig,
+                         static_cast<float *>(dst), o.staged_ld, o.rows, o.k, o.is_b, s);
+  if (o.transpose) return transpose_launch(o.ptr, o.ld, dst, o.staged_ld, o.outer, o.inner, es, s);
+  return repack_launch(o.ptr, o.ld, dst, o.staged_ld, o.outer, o.inner, es, s);
+}
+
 // Tensor maps, kernel parameters and launch of the tensor-core kernel for operands that
 // are already TMA-legal (in place or staged).
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
@@ -437,9 +467,10 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   tp.status = status;
   tp.timeout_ns = timeout_ns;
   tp.debug_flags = debug_flags;
+  tp.chunk_kblocks = kExactChunkKBlocks;
   int64_t grid = I.ctas;
   if (pl.variant.pair) {
-    const int64_t fit = tc2_max_active_clusters();
+    const int64_t fit = pl.variant.exact ? tc_exact_max_active_clusters() : tc2_max_active_clusters();
     if (fit <= 0) return GEMM_ERR_CUDA;
     if (grid / 2 > fit) grid = 2 * fit;
   }
@@ -478,8 +509,7 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   for (const OperandPlan *o : {&pl.a, &pl.b}) {
     if (!o->staged) continue;
     void *dst = static_cast<char *>(h->workspace) + o->ws_offset;
-    e = o->transpose ? transpose_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s)
-                     : repack_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s);
+    e = stage_operand(*o, dst, es, s);
     if (e != cudaSuccess) return cuda_fail(e, "stage operand");
     h->launches += 1;
     if (o == &pl.a)
@@ -746,8 +776,7 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
   for (const OperandPlan *o : {&pl.a, &pl.b}) {
     if (!o->staged) continue;
     void *dst = staging + o->ws_offset;
-    e = o->transpose ? transpose_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s)
-                     : repack_launch(o->ptr, o->ld, dst, o->staged_ld, o->outer, o->inner, es, s);
+    e = stage_operand(*o, dst, es, s);
     if (e != cudaSuccess) return cuda_fail(e, "stage operand");
     if (o == &pl.a)
       a_ptr = dst, a_ld = o->staged_ld;
@@ -782,5 +811,13 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(
   if (st != GEMM_OK) return st;
   st = make_plan(P, Options(), sms, &pl);
   if (st != GEMM_OK) return st;
+  if (pl.info.path == GEMM_PATH_TCGEN05_3XTF32 &&
+      static_cast<size_t>(pl.info.workspace_bytes) > GEMM_NOALLOC_SCRATCH_BYTES - kStaticStatusBytes) {
+    // Exact fp32 whose split operands do not fit the array: the fp32 FMA kernel needs none.
+    Options fma;
+    fma.force_path = 2;
+    st = make_plan(P, fma, sms, &pl);
+    if (st != GEMM_OK) return st;
+  }
   return execute_noalloc(scratch, device_status, P, pl, static_cast<cudaStream_t>(cuda_stream));
 }

@@ -29,6 +29,7 @@ struct TcParams {
   int *status;         // device status word
   uint64_t timeout_ns; // bounded-wait limit
   int32_t debug_flags;
+  int32_t chunk_kblocks;  // exact-fp32 kernel: K-blocks per TMEM partial sum
 };
 
 // One tensor-core kernel variant: element size of A and B (2 = f16/bf16, 4 = fp32 as tf32),
@@ -37,7 +38,8 @@ struct TcVariant {
   int esize;
   bool a_mn, b_mn;
   int block_n;
-  bool pair;  // CTA pair (cta_group::2): 256 x 256 tiles over two SMs
+  bool pair;   // CTA pair (cta_group::2): 256-row tiles over two SMs
+  bool exact;  // exact-fp32 kernel on split operands (CTA pairs, chunked fp32 sums)
 };
 
 int tc_stages(const TcVariant &v);
@@ -48,6 +50,13 @@ cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtenso
                        const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
 // Clusters of two CTAs of the pair kernel that fit on the current device at once.
 int tc2_max_active_clusters();
+// Exact-fp32 kernel (CTA pairs, 256 x 256 tiles, split tf32 operands, chunked sums).
+cudaError_t tc_exact_launch(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                            const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+int tc_exact_max_active_clusters();
+// K-blocks of 32 split products accumulated in TMEM before the exact kernel adds the
+// partial into its fp32 register sums.
+constexpr int kExactChunkKBlocks = 4;
 
 // fp32 fused-multiply-add tile kernel (exact fp32 mode; any input dtype/layout).
 struct FmaParams {
@@ -74,6 +83,12 @@ cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld
 // `inner` lines of `outer` elements in dst (leading dim ld_dst >= outer).
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t outer, int64_t inner, int esize, cudaStream_t s);
+
+// Exact-fp32 staging: writes the K-major operand [hi | hi | lo] (A) or [hi | lo | hi] (B)
+// of R rows and 3K columns (leading dim ldd >= 3K) from an fp32 operand X[r][k] stored
+// K-contiguous (src[r*lds + k]) or not (src[k*lds + r]).
+cudaError_t split3_launch(const float *src, int64_t lds, bool k_contig, float *dst, int64_t ldd,
+                          int64_t R, int64_t K, bool is_b, cudaStream_t s);
 
 // C[i, j] = 0 for i < M, j < N.
 cudaError_t zero_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, int out_dtype,

@@ -282,6 +282,25 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
   return mbar_wait_cluster_slow(a, parity, wd);
 }
 
+// The same bounded wait, expanded in place: for callers that keep many live registers
+// (a call to the out-of-line slow path would spill them around every wait).
+__device__ __forceinline__ bool mbar_wait_cluster_inline(uint64_t *bar, uint32_t parity,
+                                                         const Watchdog &wd) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (*wd.abort_flag) return false;
+    if (global_timer_ns() - t0 > wd.timeout_ns || it > (1u << 30)) {
+      atomicCAS(wd.status, 0, kStatusTimeout);
+      *wd.abort_flag = 1;
+      __threadfence_block();
+      return false;
+    }
+  }
+}
+
 // TMA load into this CTA's shared memory whose completion is signalled on an mbarrier of
 // either CTA of the pair (`bar` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t bar,

@@ -1,0 +1,368 @@
+// tc_exact_kernel.cu -- exact-fp32 GEMM on the tensor cores (CTA pairs, chunked sums).
+//
+// Exact fp32 ("Triton matmul", "Precision": fp32 inputs need an explicit choice between
+// tf32 and full fp32 accuracy) runs on the tf32 tensor cores: split_kernel.cu writes
+// A' = [hi(A) | hi(A) | lo(A)] and B' = [hi(B) ; lo(B) ; hi(B)] so that A' B' holds the three
+// significant partial products of the split operands. The tensor cores' fp32 accumulation
+// over a long K drifts (measured on GB300: 4e-6 of sum |a b| at K = 4096, growing with K),
+// so this kernel never lets one TMEM accumulator run over more than a short chunk of K':
+// the MMA issuer alternates between two TMEM accumulators every `chunk` K-blocks, and the
+// epilogue warps add each finished chunk into fp32 registers with ordinary IEEE adds. The
+// tile's structure is otherwise the blocked matmul of "Chapter 13: The Blocked Matmul
+// Kernel", section 13.1: the register sum starts at zero once per tile, every K-chunk's
+// partial product is added to it, and the result is rounded once at the store (13.3).
+//
+// Roles (320 threads per CTA, clusters of two CTAs, 256 x 256 tile per cluster):
+//   warp 0      TMA producer (both CTAs): 128 rows of A', 128 columns of B' per K-block;
+//   warp 1      MMA issuer (leader CTA): tcgen05.mma.cta_group::2.kind::tf32, M=256, N=256;
+//   warps 2-9   epilogue (both CTAs): warp w reads TMEM lanes 32*(w%4).. and one 128-column
+//               half of the tile, keeps 128 fp32 sums per thread, stores once per tile.
+#include "tc_common.cuh"
+
+namespace gemm_gb300 {
+namespace {
+
+using namespace tc;
+
+constexpr int kXThreads = 320;
+constexpr int kXEpiWarps = 8;
+
+struct CfgX {
+  static constexpr int BM = kTcBlockM;          // rows per CTA (256 per pair)
+  static constexpr int BN = 256;                // columns per pair tile
+  static constexpr int BN_HALF = BN / 2;        // B' columns loaded by each CTA
+  static constexpr int BK = kRowBytes / 4;      // 32 fp32 per K-block
+  static constexpr int UMMA_K = 8;              // K per tcgen05.mma.kind::tf32
+  static constexpr int K_STEPS = BK / UMMA_K;
+  static constexpr int A_BYTES = BM * BK * 4;
+  static constexpr int B_BYTES = BN_HALF * BK * 4;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = 6;
+  static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int EPI_BYTES = kXEpiWarps * kStoreBufBytes;  // one staging box per warp
+  static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int COLS = 128;  // columns per epilogue thread
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Store one warp's 32 x 128 block from registers through the 128B-swizzled staging box.
+template <int OUT>
+__device__ __forceinline__ void store_regs_tma(const float (&v)[CfgX::COLS], const CUtensorMap *tmC,
+                                               uint8_t *sb, int lane, int row0, int col0, int M,
+                                               int N) {
+  constexpr int OUT_COLS = OUT == GEMM_F32 ? 32 : 64;
+  if (row0 >= M) return;  // warp-uniform
+#pragma unroll
+  for (int b = 0; b < CfgX::COLS / OUT_COLS; ++b) {
+    if (col0 + b * OUT_COLS >= N) break;  // warp-uniform
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    const uint32_t row_addr = smem_u32(sb) + lane * kRowBytes;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t w0, w1, w2, w3;
+      if (OUT == GEMM_F32) {
+        const int c = b * 32 + ch * 4;
+        w0 = __float_as_uint(v[c]), w1 = __float_as_uint(v[c + 1]);
+        w2 = __float_as_uint(v[c + 2]), w3 = __float_as_uint(v[c + 3]);
+      } else {
+        const int c = b * 64 + ch * 8;
+        w0 = pack2<OUT>(__float_as_uint(v[c]), __float_as_uint(v[c + 1]));
+        w1 = pack2<OUT>(__float_as_uint(v[c + 2]), __float_as_uint(v[c + 3]));
+        w2 = pack2<OUT>(__float_as_uint(v[c + 4]), __float_as_uint(v[c + 5]));
+        w3 = pack2<OUT>(__float_as_uint(v[c + 6]), __float_as_uint(v[c + 7]));
+      }
+      const uint32_t dst = row_addr + ((ch ^ (lane & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w0), "r"(w1),
+                   "r"(w2), "r"(w3)
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, smem_u32(sb), col0 + b * OUT_COLS, row0);
+      bulk_commit_group();
+    }
+  }
+}
+
+// Store one thread's row segment from registers with plain masked stores.
+template <int OUT>
+__device__ __forceinline__ void store_regs_direct(const float (&v)[CfgX::COLS], const TcParams &p,
+                                                  int row, int col0) {
+  if (row >= p.M || col0 >= p.N) return;
+  const int n = min(CfgX::COLS, p.N - col0);
+  const int64_t base = static_cast<int64_t>(row) * p.ldc + col0;
+#pragma unroll
+  for (int j = 0; j < CfgX::COLS; ++j) {
+    if (j < n) {
+      if (OUT == GEMM_F32)
+        reinterpret_cast<float *>(p.C)[base + j] = v[j];
+      else if (OUT == GEMM_BF16)
+        reinterpret_cast<__nv_bfloat16 *>(p.C)[base + j] = __float2bfloat16_rn(v[j]);
+      else
+        reinterpret_cast<__half *>(p.C)[base + j] = __float2half_rn(v[j]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kXThreads, 1)
+    tc_exact_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using G = CfgX;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::BAR_OFFSET);
+  uint64_t *empty = full + G::STAGES;
+  uint64_t *tmem_full = empty + G::STAGES;
+  uint64_t *tmem_empty = tmem_full + 2;
+  uint64_t *drain = tmem_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int chunk = p.chunk_kblocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 2 * kXEpiWarps);  // every epilogue warp of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (p.tma_store) prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), G::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int cluster_id = blockIdx.x / 2;
+  const int num_clusters = gridDim.x / 2;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+        int pm, pn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+        const int m0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM;
+        const int n0 = pn * G::BN + static_cast<int>(rank) * G::BN_HALF;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
+          const uint32_t a_dst = smem_u32(smem + stage * G::STAGE_BYTES);
+          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+          tma_load_2d_pair(a_dst, &tmA, fb, kb * G::BK, m0);
+          tma_load_2d_pair(a_dst + G::A_BYTES, &tmB, fb, kb * G::BK, n0);
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+        uint32_t d_tmem = 0;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          const int in_chunk = kb % chunk;
+          if (in_chunk == 0) {  // a fresh accumulator for this chunk of K'
+            if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, wd)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + acc * G::BN;
+          }
+          if (!mbar_wait_cluster(&full[stage], phase, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
+          const uint32_t b_base = a_base + G::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < G::K_STEPS; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            mma_tf32_pair(d_tmem, ad, bd, p.idesc, (in_chunk | kk) != 0);
+          }
+          mma_commit_pair_multicast(&empty[stage], 0x3);
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (in_chunk == chunk - 1 || kb == p.k_blocks - 1) {  // chunk done: hand it over
+            mma_commit_pair_multicast(&tmem_full[acc], 0x3);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+          }
+        }
+      }
+      mma_commit_pair(drain);
+      drain_wait(drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue (both CTAs)
+    const int e = warp - 2;
+    const int quarter = warp & 3;
+    const int half = e >> 2;  // which 128 columns of the tile
+    uint8_t *sb = smem + G::EPI_OFFSET + e * kStoreBufBytes;
+    uint32_t acc = 0, acc_phase = 0;
+    const int chunks = (p.k_blocks + chunk - 1) / chunk;
+    bool ok = true;
+    for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      float sum[G::COLS];
+#pragma unroll
+      for (int j = 0; j < G::COLS; ++j) sum[j] = 0.0f;  // the tile's sum starts at zero once
+      for (int c = 0; c < chunks; ++c) {
+        bool got = mbar_wait_cluster_inline(&tmem_full[acc], acc_phase, wd);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           acc * G::BN + half * G::COLS;
+#pragma unroll
+        for (int q = 0; q < G::COLS / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t + q * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum[q * 32 + j] += __uint_as_float(r[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) break;
+      int pm, pn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+      const int row0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM + quarter * 32;
+      const int col0 = pn * G::BN + half * G::COLS;
+      if (p.tma_store) {
+        if (p.out_dtype == GEMM_BF16)
+          store_regs_tma<GEMM_BF16>(sum, &tmC, sb, lane, row0, col0, p.M, p.N);
+        else if (p.out_dtype == GEMM_F16)
+          store_regs_tma<GEMM_F16>(sum, &tmC, sb, lane, row0, col0, p.M, p.N);
+        else
+          store_regs_tma<GEMM_F32>(sum, &tmC, sb, lane, row0, col0, p.M, p.N);
+      } else {
+        if (p.out_dtype == GEMM_BF16)
+          store_regs_direct<GEMM_BF16>(sum, p, row0 + lane, col0);
+        else if (p.out_dtype == GEMM_F16)
+          store_regs_direct<GEMM_F16>(sum, p, row0 + lane, col0);
+        else
+          store_regs_direct<GEMM_F32>(sum, p, row0 + lane, col0);
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000) __nanosleep(1000);
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int tc_exact_max_active_clusters() {
+  static int cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(tc_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           CfgX::SMEM_BYTES) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kXThreads, 1, 1);
+  cfg.dynamicSmemBytes = CfgX::SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_exact_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t tc_exact_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                            const TcParams &p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(tc_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       CfgX::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kXThreads, 1, 1);
+  cfg.dynamicSmemBytes = CfgX::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_exact_kernel, tmA, tmB, tmC, p);
+}
+
+}  // namespace gemm_gb300

@@ -34,10 +34,14 @@
  * with round-to-nearest-even. K == 0 writes zeros (the empty sum). M == 0 or
  * N == 0 is a no-op returning GEMM_OK.
  *
- * Precision (fp32 inputs only): GEMM_PREC_DEFAULT means GEMM_PREC_EXACT_FP32
- * (fp32 fused multiply-adds); GEMM_PREC_TF32 runs the tensor cores on tf32
- * operands (the low 13 mantissa bits of each fp32 input are ignored). 16-bit
- * inputs accept only GEMM_PREC_DEFAULT.
+ * Precision (fp32 inputs only): GEMM_PREC_DEFAULT means GEMM_PREC_EXACT_FP32;
+ * GEMM_PREC_TF32 runs the tensor cores on tf32 operands (the low 13 mantissa bits
+ * of each fp32 input are ignored; max |err| <= 2e-3 * sum_k |a_ik b_kj|).
+ * GEMM_PREC_EXACT_FP32 keeps fp32 accuracy (max |err| <= 1e-6 * sum_k |a_ik b_kj|
+ * on the library's tests): each operand is split into two tf32 parts and the
+ * three significant partial products run on the tensor cores, accumulating in
+ * fp32 (tiny problems use fp32 fused multiply-adds). 16-bit inputs accept only
+ * GEMM_PREC_DEFAULT.
  *
  * Errors: checks on the host return a status and launch nothing. Work is
  * asynchronous on the given stream, so a GEMM_OK return means "launched";
@@ -73,7 +77,7 @@ typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2 } gemm_dtype_t;
 typedef enum {
   GEMM_PREC_DEFAULT = 0,   /* exact fp32 for fp32 inputs; the only mode for 16-bit inputs */
   GEMM_PREC_TF32 = 1,      /* fp32 inputs on the tf32 tensor-core path */
-  GEMM_PREC_EXACT_FP32 = 2 /* fp32 inputs, fp32 fused multiply-add accumulation */
+  GEMM_PREC_EXACT_FP32 = 2 /* fp32 inputs at fp32 accuracy (split-tf32 tensor cores) */
 } gemm_precision_t;
 
 typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
@@ -135,7 +139,7 @@ GEMM_API const char *gemm_strerror(gemm_status_t s);
 
 typedef enum {
   GEMM_OPT_WAIT_TIMEOUT_US = 0, /* device bounded-wait limit in microseconds (default 2000000) */
-  GEMM_OPT_FORCE_PATH = 1,      /* 0 auto, 1 tensor-core path, 2 fp32 FMA path (exact fp32 only) */
+  GEMM_OPT_FORCE_PATH = 1,      /* 0 auto, 1 tensor cores, 2 fp32 FMA kernel (any input dtype) */
   GEMM_OPT_GROUP_M = 2,         /* tile rows per raster group of the persistent schedule (>= 1) */
   GEMM_OPT_MAX_CTAS = 3,        /* cap on persistent CTAs (0 = one per SM) */
   GEMM_OPT_FAULT_STALL_PRODUCER = 4, /* test hook: the tensor-core kernel's loader issues
@@ -159,7 +163,9 @@ typedef enum {
   GEMM_PATH_NONE = 0,      /* nothing to do (M == 0 or N == 0) */
   GEMM_PATH_ZERO_FILL = 1, /* K == 0: C is set to zero */
   GEMM_PATH_TCGEN05 = 2,   /* TMA + mbarrier pipeline + tcgen05.mma, TMEM accumulator */
-  GEMM_PATH_FMA = 3        /* fp32 fused multiply-add tiles (exact fp32 mode) */
+  GEMM_PATH_FMA = 3,       /* fp32 fused multiply-add tiles (exact fp32, tiny problems) */
+  GEMM_PATH_TCGEN05_3XTF32 = 4 /* exact fp32 on the tensor cores: operands split into tf32
+                                  hi/lo parts, three products in one fp32 accumulator */
 } gemm_path_t;
 
 typedef struct {

@@ -88,6 +88,22 @@ def test_ragged_sweep_all_216(h):
     assert worst < 1e-2
 
 
+def test_ragged_sweep_fp32_exact_all_216(h):
+    # fp32 inputs in exact mode: the accuracy gate for running exact fp32 on the tensor
+    # cores as three tf32 products (max |err| / sum |a b| <= 1e-6 on every combination).
+    worst, failures = 0.0, []
+    for (M, N, K) in W.ragged_combos():
+        p = W.ragged(M, N, K, dtype="f32")
+        c = run_gpu(h, p)
+        C64, D = oracle_rows(p)
+        err = rel_err(c, C64, D)
+        worst = max(worst, err)
+        if err > tolerance(p):
+            failures.append(((M, N, K), err))
+    assert not failures, failures[:10]
+    print("worst exact-mode relative error over the sweep: %.3g" % worst)
+
+
 @pytest.mark.parametrize("M,N,K", [(1025, 17, 1023), (127, 1000, 1025), (17, 1023, 1000),
                                    (1, 1025, 127)])
 def test_ragged_guard_bands(h, M, N, K):
@@ -149,6 +165,21 @@ def test_integer_inputs_bit_exact(h_tiles, dtype, precision, a_layout, b_layout)
         ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
         assert torch.equal(c.cpu().to(torch.int64), ref), (M, N, K)
         assert torch.equal(c.cpu(), ref.to(torch.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_fma_kernel_integer_exact(h, dtype):
+    import dense_tiled_gemm_05_gb300 as g
+    h2 = g.Gemm(0)
+    h2.set_option("force_path", 2)
+    for n, (M, N, K) in enumerate([(1, 1, 1), (129, 257, 65), (300, 200, 1025), (8, 8, 8)]):
+        for al, bl in itertools.product(["row", "col"], repeat=2):
+            p = W.integer_problem(M, N, K, dtype, seed=300 + n, a_layout=al, b_layout=bl)
+            assert h2.plan(to_device(p.A), to_device(p.B), out_dtype="f32",
+                           precision=p.precision)["path"] == "fma"
+            c = run_gpu(h2, p)
+            assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    h2.close()
 
 
 @pytest.mark.parametrize("out_dtype", ["f16", "bf16", "f32"])
@@ -268,10 +299,15 @@ def test_bf16_4096_col_major_b(h):
     assert s_err <= tol, s_err
 
 
-@pytest.mark.parametrize("precision", ["tf32", "exact"])
-def test_fp32_4096_modes(h, precision):
+@pytest.mark.parametrize("precision,force_path", [("tf32", 0), ("exact", 0), ("exact", 2)],
+                         ids=["tf32", "exact_3xtf32", "exact_fma"])
+def test_fp32_4096_modes(h, precision, force_path):
+    import dense_tiled_gemm_05_gb300 as g
     p = W.fp32_square(4096, precision)
-    c = run_gpu(h, p)
+    h2 = g.Gemm(0)
+    h2.set_option("force_path", force_path)
+    c = run_gpu(h2, p)
+    h2.close()
     err = check_sampled(p, c)
     assert err <= tolerance(p), (precision, err)
     s_err, tol = check_sums(p, c)

@@ -160,13 +160,15 @@ def ragged_combos():
     return list(itertools.product(RAGGED_SIZES, RAGGED_SIZES, RAGGED_SIZES))
 
 
-def ragged(M, N, K, seed=None):
-    """fp16 A[M,K] @ B[K,N], uniform[-1, 1], row-major with tight leading dims, fp32 out."""
+def ragged(M, N, K, seed=None, dtype="f16"):
+    """A[M,K] @ B[K,N] (fp16 by default), uniform[-1, 1], row-major with tight leading dims,
+    fp32 out; fp32 inputs run in exact mode."""
     if seed is None:
         seed = 1000 + ragged_combos().index((M, N, K))
-    A = make_operand(M, K, "f16", "row", 2 * seed)
-    B = make_operand(K, N, "f16", "row", 2 * seed + 1)
-    return Problem("ragged_%dx%dx%d" % (M, N, K), A, B, "f32", "default")
+    A = make_operand(M, K, dtype, "row", 2 * seed)
+    B = make_operand(K, N, dtype, "row", 2 * seed + 1)
+    prec = "exact" if dtype == "f32" else "default"
+    return Problem("ragged_%s_%dx%dx%d" % (dtype, M, N, K), A, B, "f32", prec)
 
 
 def bf16_square(n, seed=2, b_layout="col"):
