@@ -32,7 +32,7 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
           6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_DEVICE"}
 OPTIONS = {"wait_timeout_us": 0, "force_path": 1, "group_m": 2, "max_ctas": 3,
            "fault_stall_producer": 4, "force_staging": 5, "cta_pair": 6,
-           "block_n": 7}
+           "block_n": 7, "exact_chunk": 8}
 PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma", 4: "tcgen05_3xtf32"}
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 _DT_NAMES = {"f32": F32, "f16": F16, "bf16": BF16}
@@ -41,7 +41,7 @@ _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
-           "gemm_version", "gemm_run_noalloc")
+           "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments")
 
 
 class GemmError(RuntimeError):
@@ -106,6 +106,9 @@ def lib():
                 L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32,
                                                i32, i32, i32, i32, vp, vp]
                 L.gemm_run_noalloc.restype = i32
+                L.gemm_schedule_segments.argtypes = [i32, i32, i32, i32, i32,
+                                                     ctypes.POINTER(ctypes.c_int32), vp, i32]
+                L.gemm_schedule_segments.restype = i32
                 L.gemm_version.argtypes = []
                 L.gemm_version.restype = ctypes.c_char_p
                 _lib = L
@@ -290,6 +293,29 @@ def matmul_host(a, b, out=None, out_dtype=None, precision="default", device=None
     if out is None:
         out = torch.empty(dc.shape, dtype=dc.dtype, pin_memory=True)
     out.copy_(dc, non_blocking=True)
+    return out
+
+
+class Segment(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int32), ("kb_begin", ctypes.c_int32),
+                ("kb_end", ctypes.c_int32), ("role", ctypes.c_int32),
+                ("first_src", ctypes.c_int32), ("last_src", ctypes.c_int32)]
+
+
+def schedule(tiles, k_blocks, slots, stream_k=True):
+    """Host-only tile schedule: per worker, (whole tiles, [split pieces as tuples])."""
+    out = []
+    for s in range(slots):
+        whole = ctypes.c_int32()
+        n = lib().gemm_schedule_segments(tiles, k_blocks, slots, int(stream_k), s,
+                                         ctypes.byref(whole), None, 0)
+        if n < 0:
+            raise ValueError("invalid schedule arguments")
+        buf = (Segment * max(n, 1))()
+        lib().gemm_schedule_segments(tiles, k_blocks, slots, int(stream_k), s,
+                                     ctypes.byref(whole), buf, n)
+        out.append((whole.value, [(x.tile, x.kb_begin, x.kb_end, x.role, x.first_src,
+                                   x.last_src) for x in buf[:n]]))
     return out
 
 

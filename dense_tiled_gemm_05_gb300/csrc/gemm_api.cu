@@ -18,6 +18,7 @@
 
 #include "gemm.h"
 #include "internal.h"
+#include "sk_schedule.h"
 
 using namespace gemm_gb300;
 
@@ -37,6 +38,7 @@ struct gemm_handle_s {
   int force_staging = 0;
   int cta_pair = 0;  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
   int block_n = 0;   // 0 auto, else 128 or 256
+  int exact_chunk = 0;  // 0 default
 };
 
 namespace {
@@ -430,7 +432,7 @@ cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t 
 // are already TMA-legal (in place or staged).
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
                         const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,
-                        int group_m, int debug_flags, cudaStream_t s) {
+                        int group_m, int debug_flags, int exact_chunk, cudaStream_t s) {
   const gemm_plan_info_t &I = pl.info;
   const int es = esize_of(P.in_dtype);
   const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
@@ -467,7 +469,7 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   tp.status = status;
   tp.timeout_ns = timeout_ns;
   tp.debug_flags = debug_flags;
-  tp.chunk_kblocks = kExactChunkKBlocks;
+  tp.chunk_kblocks = exact_chunk > 0 ? exact_chunk : exact_chunk_kblocks(I.k_iters);
   int64_t grid = I.ctas;
   if (pl.variant.pair) {
     const int64_t fit = pl.variant.exact ? tc_exact_max_active_clusters() : tc2_max_active_clusters();
@@ -518,7 +520,7 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
       b_ptr = dst, b_ld = o->staged_ld;
   }
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
-                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, s);
+                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, h->exact_chunk, s);
   if (st != GEMM_OK) return st;
   h->launches += 1;
   return GEMM_OK;
@@ -529,6 +531,25 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
 extern "C" {
 
 GEMM_API const char *gemm_version(void) { return kVersion; }
+
+GEMM_API int32_t gemm_schedule_segments(int32_t tiles, int32_t k_blocks, int32_t slots,
+                                        int32_t stream_k, int32_t slot, int32_t *whole_tiles,
+                                        gemm_segment_t *out, int32_t max_out) {
+  if (tiles < 0 || k_blocks < 1 || slots < 1 || slot < 0 || slot >= slots || max_out < 0)
+    return -1;
+  const SkSchedule S =
+      sk_make(tiles, k_blocks, slots, sk_dp_tiles(tiles, k_blocks, slots, stream_k != 0));
+  if (whole_tiles) *whole_tiles = sk_dp_count(S, slot);
+  int32_t n = 0;
+  for (int64_t u = sk_begin(S, slot), hi = sk_begin(S, slot + 1); u < hi; ++n) {
+    SkSegment seg;
+    u = sk_segment_at(S, slot, u, &seg);
+    if (out && n < max_out)
+      out[n] = gemm_segment_t{seg.tile, seg.kb_begin, seg.kb_end, seg.role, seg.first_src,
+                              seg.last_src};
+  }
+  return n;
+}
 
 GEMM_API const char *gemm_strerror(gemm_status_t s) {
   switch (s) {
@@ -612,6 +633,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
     case GEMM_OPT_CTA_PAIR:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_EXACT_CHUNK:
+      if (v < 0 || v > 64) return GEMM_ERR_INVALID_ARG;
+      h->exact_chunk = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_BLOCK_N:
       if (v != 0 && v != 128 && v != 256) return GEMM_ERR_INVALID_ARG;
@@ -785,7 +810,7 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
   }
   const Options defaults;
   return launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, status, gemm_handle_s().timeout_us * 1000ull,
-                   defaults.group_m, 0, s);
+                   defaults.group_m, 0, 0, s);
 }
 
 }  // namespace

@@ -54,9 +54,15 @@ int tc2_max_active_clusters();
 cudaError_t tc_exact_launch(const CUtensorMap &tmA, const CUtensorMap &tmB,
                             const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
 int tc_exact_max_active_clusters();
-// K-blocks of 32 split products accumulated in TMEM before the exact kernel adds the
-// partial into its fp32 register sums.
-constexpr int kExactChunkKBlocks = 4;
+// K-blocks of 32 split products the exact kernel accumulates in TMEM before adding the
+// partial into its fp32 register sums. The tensor cores' accumulation keeps fewer bits
+// than an IEEE fp32 add, and its error relative to sum |a b| is largest for short K, so
+// short products use short chunks; long ones use up to 16 K-blocks (longer chunks only
+// saved ~1 % more time on GB300).
+inline int exact_chunk_kblocks(int64_t k_blocks) {
+  const int64_t c = k_blocks / 24;
+  return static_cast<int>(c < 1 ? 1 : c > 16 ? 16 : c);
+}
 
 // fp32 fused-multiply-add tile kernel (exact fp32 mode; any input dtype/layout).
 struct FmaParams {

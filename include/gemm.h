@@ -148,7 +148,9 @@ typedef enum {
   GEMM_OPT_FORCE_STAGING = 5,   /* 1 = stage A and B through the workspace even when aligned */
   GEMM_OPT_CTA_PAIR = 6,        /* tensor-core tiles: 0 auto, 1 single-CTA (128 rows),
                                    2 CTA-pair (256 rows, cta_group::2 on two SMs) */
-  GEMM_OPT_BLOCK_N = 7          /* tensor-core tile width: 0 auto, 128 or 256 */
+  GEMM_OPT_BLOCK_N = 7,         /* tensor-core tile width: 0 auto, 128 or 256 */
+  GEMM_OPT_EXACT_CHUNK = 8      /* exact fp32: 32-long K-blocks summed in TMEM before each
+                                   fp32 register add (0 = by K: k_blocks/24 in [1, 16]; 1..64) */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
@@ -192,6 +194,27 @@ GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t 
                                  gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
                                  gemm_layout_t a_layout, gemm_layout_t b_layout,
                                  int32_t sm_count, gemm_plan_info_t *info);
+
+/* One piece of a worker's share of the output tiles (see gemm_schedule_segments). */
+typedef struct {
+  int32_t tile;      /* output tile index in the grouped raster order */
+  int32_t kb_begin;  /* first K-block of the tile this piece computes */
+  int32_t kb_end;    /* one past its last K-block */
+  int32_t role;      /* 0 whole tile, 1 partial (fp32 sum to the workspace), 2 owner (adds
+                        the partials of workers first_src..last_src, then stores) */
+  int32_t first_src, last_src;
+} gemm_segment_t;
+
+/* Host-only view of the tile schedule of the tensor-core kernels: `tiles` output tiles of
+ * `k_blocks` K-blocks each on `slots` persistent workers. With stream_k == 0 every tile is
+ * done whole, round-robin. Otherwise the tiles of the last, partly filled rounds are cut
+ * into K-blocks and shared equally (split-K with a fixed-order reduction: every partial is
+ * added by the owner of its tile in increasing worker order). Writes worker `slot`'s
+ * round-robin tile count to *whole_tiles and up to max_out of its split pieces to out;
+ * returns the number of split pieces, or -1 for invalid arguments. */
+GEMM_API int32_t gemm_schedule_segments(int32_t tiles, int32_t k_blocks, int32_t slots,
+                                        int32_t stream_k, int32_t slot, int32_t *whole_tiles,
+                                        gemm_segment_t *out, int32_t max_out);
 
 /* Library version as "major.minor.patch". */
 GEMM_API const char *gemm_version(void);
