@@ -32,7 +32,7 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
           6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_DEVICE"}
 OPTIONS = {"wait_timeout_us": 0, "force_path": 1, "group_m": 2, "max_ctas": 3,
            "fault_stall_producer": 4, "force_staging": 5, "cta_pair": 6,
-           "block_n": 7, "exact_chunk": 8}
+           "block_n": 7, "exact_chunk": 8, "stream_k": 9}
 PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma", 4: "tcgen05_3xtf32"}
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 _DT_NAMES = {"f32": F32, "f16": F16, "bf16": BF16}
@@ -58,7 +58,7 @@ class PlanInfo(ctypes.Structure):
                 ("stage_b", ctypes.c_int32), ("a_mn_major", ctypes.c_int32),
                 ("b_mn_major", ctypes.c_int32), ("tma_store", ctypes.c_int32),
                 ("ctas", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("cta_pair", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("split_tiles", ctypes.c_int32)]
 
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}

@@ -39,6 +39,11 @@ struct gemm_handle_s {
   int cta_pair = 0;  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
   int block_n = 0;   // 0 auto, else 128 or 256
   int exact_chunk = 0;  // 0 default
+  int stream_k = 0;     // 0 auto (on), 1 off
+  // split-K workspace of the CTA-pair kernel: partial tiles and flags
+  void *sk_ws = nullptr;
+  size_t sk_ws_bytes = 0;
+  int32_t sk_epoch = 0;
 };
 
 namespace {
@@ -121,6 +126,7 @@ struct Problem {
 
 struct Options {
   int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
+  int stream_k = 0;
 };
 
 // An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
@@ -243,13 +249,19 @@ OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, 
 // re-reads its 128 x 16 slice of A from shared memory, so narrow MMAs are starved of
 // shared-memory bandwidth); it wins only when it fills the machine much better, e.g.
 // when N itself is at most 128.
-int pick_block_n(int64_t M, int64_t N, bool pair, int sm_count) {
+int pick_block_n(int64_t M, int64_t N, int64_t k_blocks, bool pair, bool stream_k, int sm_count) {
   const int64_t rows = pair ? 2 * kTcBlockM : kTcBlockM;
   const int64_t slots = pair ? (sm_count > 1 ? sm_count / 2 : 1) : (sm_count > 0 ? sm_count : 1);
   const int64_t tiles_m = (M + rows - 1) / rows;
   auto cost = [&](int64_t bn, double per_column) {
     const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
-    return static_cast<double>((tiles + slots - 1) / slots) * static_cast<double>(bn) * per_column;
+    // With a split-K share the last round is spread over every slot: fractional rounds.
+    const bool split = pair && stream_k &&
+                       sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(k_blocks),
+                                   static_cast<int32_t>(slots), true) < tiles;
+    const double rounds = split ? static_cast<double>(tiles) / static_cast<double>(slots)
+                                : static_cast<double>((tiles + slots - 1) / slots);
+    return rounds * static_cast<double>(bn) * per_column;
   };
   return cost(128, 1.5) < cost(256, 1.0) ? 128 : 256;
 }
@@ -305,8 +317,10 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // CTA pairs (256-row tiles on two SMs) halve the shared-memory and L2 traffic per
   // flop; a problem no taller than one 128-row tile keeps single-CTA tiles.
   pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM);
-  pl.variant.block_n = opt.block_n ? opt.block_n
-                                   : pick_block_n(P.M, P.N, pl.variant.pair, sm_count);
+  pl.variant.block_n =
+      opt.block_n ? opt.block_n
+                  : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
+                                 opt.stream_k == 0 && !split, sm_count);
   if (split) {  // the exact-fp32 kernel has one shape: CTA pairs, 256 x 256 tiles
     pl.variant.exact = true;
     pl.variant.pair = true;
@@ -332,9 +346,13 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   const int64_t tiles = I.grid_m * I.grid_n;
   if (pl.variant.pair) {
     // One cluster of two CTAs per tile slot; the launch clamps to the clusters that fit.
+    // With a split-K share every cluster takes part, even when there are fewer tiles.
     int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
     if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
-    I.ctas = 2 * (tiles < clusters ? tiles : clusters);
+    const bool split = !pl.variant.exact && opt.stream_k == 0 &&
+                       sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(I.k_iters),
+                                   static_cast<int32_t>(clusters), true) < tiles;
+    I.ctas = 2 * (split || tiles > clusters ? clusters : tiles);
   } else {
     int64_t ctas = sm_count > 0 ? sm_count : 1;
     if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
@@ -342,6 +360,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   }
   I.workspace_bytes = static_cast<int64_t>(cursor);
   I.cta_pair = pl.variant.pair ? 1 : 0;
+  if (pl.variant.pair && !pl.variant.exact && opt.stream_k == 0) {
+    const int32_t slots = static_cast<int32_t>(I.ctas / 2);
+    const int32_t t = static_cast<int32_t>(tiles);
+    I.split_tiles = t - sk_dp_tiles(t, static_cast<int32_t>(I.k_iters), slots, true);
+  }
   *out = pl;
   return GEMM_OK;
 }
@@ -416,6 +439,7 @@ Options options_of(gemm_handle_t h) {
     o.force_staging = h->force_staging;
     o.cta_pair = h->cta_pair;
     o.block_n = h->block_n;
+    o.stream_k = h->stream_k;
   }
   return o;
 }
@@ -430,14 +454,45 @@ cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t 
 
 // Tensor maps, kernel parameters and launch of the tensor-core kernel for operands that
 // are already TMA-legal (in place or staged).
+// Split-K context of a launch: a workspace provider (null = split-K off).
+struct SplitK {
+  gemm_handle_t h = nullptr;
+};
+
+gemm_status_t ensure_sk_workspace(gemm_handle_t h, size_t bytes, size_t flag_bytes,
+                                  cudaStream_t s) {
+  if (bytes <= h->sk_ws_bytes) return GEMM_OK;
+  if (h->sk_ws) {
+    cudaFree(h->sk_ws);
+    h->sk_ws = nullptr;
+    h->sk_ws_bytes = 0;
+  }
+  void *p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_MEMORY;
+  }
+  // Flags start at 0 and every launch uses a fresh non-zero epoch, so stale flags of
+  // earlier launches never match.
+  if (cudaMemsetAsync(p, 0, flag_bytes, s) != cudaSuccess) {
+    cudaFree(p);
+    return GEMM_ERR_CUDA;
+  }
+  h->sk_ws = p;
+  h->sk_ws_bytes = bytes;
+  return GEMM_OK;
+}
+
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
                         const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,
-                        int group_m, int debug_flags, int exact_chunk, cudaStream_t s) {
+                        int group_m, int debug_flags, int exact_chunk, SplitK sk,
+                        cudaStream_t s) {
   const gemm_plan_info_t &I = pl.info;
   const int es = esize_of(P.in_dtype);
   const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
-  CUtensorMap tmA, tmB, tmC;
+  CUtensorMap tmA, tmB, tmC, tmP;
   std::memset(&tmC, 0, sizeof tmC);
+  std::memset(&tmP, 0, sizeof tmP);
   // K-major operand: box = (one 128-byte row of K) x (the CTA's rows of the tile);
   // MN-major operand: box = (one 128-byte row of M or N) x (the stage's K rows).
   const uint32_t cta_rows_a = kTcBlockM;
@@ -476,7 +531,30 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
     if (fit <= 0) return GEMM_ERR_CUDA;
     if (grid / 2 > fit) grid = 2 * fit;
   }
-  const cudaError_t e = tc_launch(pl.variant, tmA, tmB, tmC, tp, static_cast<int>(grid), s);
+  // Split-K share of the last rounds (CTA-pair kernel): whole tiles otherwise.
+  const int32_t tiles = tp.tiles_m * tp.tiles_n;
+  tp.sk_dp_tiles = tiles;
+  if (pl.variant.pair && !pl.variant.exact && sk.h) {
+    const int32_t slots = static_cast<int32_t>(grid / 2);
+    tp.sk_dp_tiles = sk_dp_tiles(tiles, tp.k_blocks, slots, true);
+    if (tp.sk_dp_tiles < tiles) {
+      const size_t flag_bytes = static_cast<size_t>(slots) * 2 * 4 * sizeof(int);
+      const size_t flag_region = (flag_bytes + 255) / 256 * 256;
+      const size_t part_bytes =
+          static_cast<size_t>(slots) * 2 * kTcBlockM * pl.variant.block_n * sizeof(float);
+      gemm_status_t st = ensure_sk_workspace(sk.h, flag_region + part_bytes, flag_region, s);
+      if (st != GEMM_OK) return st;
+      tp.sk_flags = static_cast<int *>(sk.h->sk_ws);
+      tp.sk_partials = reinterpret_cast<float *>(static_cast<char *>(sk.h->sk_ws) + flag_region);
+      // partial tiles: rows [worker][cta rank][128], block_n fp32 columns; 32 x 32 boxes
+      if (!encode_2d(&tmP, GEMM_F32, tp.sk_partials, pl.variant.block_n,
+                     static_cast<int64_t>(slots) * 2 * kTcBlockM, pl.variant.block_n, 32, 32))
+        return GEMM_ERR_CUDA;
+      sk.h->sk_epoch = sk.h->sk_epoch == INT32_MAX ? 1 : sk.h->sk_epoch + 1;
+      tp.sk_epoch = sk.h->sk_epoch;
+    }
+  }
+  const cudaError_t e = tc_launch(pl.variant, tmA, tmB, tmC, tmP, tp, static_cast<int>(grid), s);
   return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "tcgen05 launch");
 }
 
@@ -519,8 +597,10 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
     else
       b_ptr = dst, b_ld = o->staged_ld;
   }
+  SplitK sk;
+  if (h->stream_k == 0) sk.h = h;
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
-                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, h->exact_chunk, s);
+                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, h->exact_chunk, sk, s);
   if (st != GEMM_OK) return st;
   h->launches += 1;
   return GEMM_OK;
@@ -599,6 +679,7 @@ GEMM_API void gemm_destroy(gemm_handle_t h) {
   DeviceGuard g(h->device);
   cudaDeviceSynchronize();
   if (h->workspace) cudaFree(h->workspace);
+  if (h->sk_ws) cudaFree(h->sk_ws);
   if (h->status) cudaFree(h->status);
   delete h;
 }
@@ -633,6 +714,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
     case GEMM_OPT_CTA_PAIR:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_STREAM_K:
+      if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
+      h->stream_k = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_EXACT_CHUNK:
       if (v < 0 || v > 64) return GEMM_ERR_INVALID_ARG;
@@ -810,7 +895,7 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
   }
   const Options defaults;
   return launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, status, gemm_handle_s().timeout_us * 1000ull,
-                   defaults.group_m, 0, 0, s);
+                   defaults.group_m, 0, 0, SplitK(), s);
 }
 
 }  // namespace

@@ -30,6 +30,11 @@ struct TcParams {
   uint64_t timeout_ns; // bounded-wait limit
   int32_t debug_flags;
   int32_t chunk_kblocks;  // exact-fp32 kernel: K-blocks per TMEM partial sum
+  // split-K share of the last rounds (CTA-pair kernel; see sk_schedule.h)
+  int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
+  float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32
+  int *sk_flags;          // [worker][cta rank][4 epilogue warps]
+  int32_t sk_epoch;       // value this launch's writers store in their flags
 };
 
 // One tensor-core kernel variant: element size of A and B (2 = f16/bf16, 4 = fp32 as tf32),
@@ -43,11 +48,14 @@ struct TcVariant {
 };
 
 int tc_stages(const TcVariant &v);
+// tmP: the split-K partial tiles as a 2D fp32 tensor (CTA-pair kernel only).
 cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                      const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+                      const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p, int grid,
+                      cudaStream_t s);
 // CTA-pair kernel: grid counts CTAs (twice the clusters).
 cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+                       const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p, int grid,
+                       cudaStream_t s);
 // Clusters of two CTAs of the pair kernel that fit on the current device at once.
 int tc2_max_active_clusters();
 // Exact-fp32 kernel (CTA pairs, 256 x 256 tiles, split tf32 operands, chunked sums).

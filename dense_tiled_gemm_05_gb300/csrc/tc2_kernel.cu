@@ -38,18 +38,22 @@ struct Cfg2 {
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * 2 * kStoreBufBytes;
   static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int NUM_BARS = 2 * STAGES + 9;  // + one partial-load barrier per epilogue warp
+  static constexpr int OWNER_SLICE = 48 * 1024;     // stage bytes an owner warp borrows
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(kEpiWarps * OWNER_SLICE <= STAGES * STAGE_BYTES, "owner slices fit the stages");
+  static_assert(BN * 32 * 4 <= OWNER_SLICE, "a warp's partial rows fit its slice");
 };
 
 template <int ESIZE, bool A_MN, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmP, const TcParams p) {
   using G = Cfg2<ESIZE, A_MN, B_MN, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -59,7 +63,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *tmem_full = empty + G::STAGES;
   uint64_t *tmem_empty = tmem_full + 2;
   uint64_t *drain = tmem_empty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *part_bar = drain + 1;  // [kEpiWarps]: split-K partial loads of the owner warps
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(part_bar + kEpiWarps);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -77,6 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_empty[b], 2 * kEpiWarps);  // one arrive per epilogue warp, both CTAs
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(&part_bar[w], 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -92,21 +98,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
-  const int num_tiles = p.tiles_m * p.tiles_n;
   const int cluster_id = blockIdx.x / 2;
   const int num_clusters = gridDim.x / 2;
+  // Whole tiles round-robin over the clusters, then the split-K share of the last rounds.
+  const SkSchedule sched = sk_make(p.tiles_m * p.tiles_n, p.k_blocks, num_clusters, p.sk_dp_tiles);
 
   if (warp == 0) {
     // ------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
-      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      WorkIter work(sched, cluster_id);
+      SkSegment seg;
+      while (ok && work.next(seg)) {
         int pm, pn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+        tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
         const int m0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM;
         const int n0 = pn * G::BN + static_cast<int>(rank) * G::BN_HALF;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
@@ -143,11 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (leader && lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      WorkIter work(sched, cluster_id);
+      SkSegment seg;
+      while (ok && work.next(seg)) {
         if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, wd)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase, wd)) {
             ok = false;
             break;
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd =
                 B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
                      : sdesc_sw128(b_base + kk * 32, 16, 1024);
-            const uint32_t accumulate = (kb | kk) != 0;
+            const uint32_t accumulate = (kb != seg.kb_begin) || kk != 0;
             if (ESIZE == 2)
               mma_f16_pair(d_tmem, ad, bd, p.idesc, accumulate);
             else
@@ -190,30 +201,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *bufs = smem + G::EPI_OFFSET + (warp - 2) * 2 * kStoreBufBytes;
     int buf = 0;
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      bool ok = mbar_wait_cluster(&tmem_full[acc], acc_phase, wd);
+    WorkIter work(sched, cluster_id);
+    SkSegment seg;
+    const int e = warp - 2;       // epilogue warp index
+    uint32_t part_phase = 0;      // parity of this warp's partial-load barrier
+    bool ok = true;
+    while (ok && work.next(seg)) {
+      ok = mbar_wait_cluster(&tmem_full[acc], acc_phase, wd);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       int pm, pn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+      tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
       const int row0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM + quarter * 32;
       const int n0 = pn * G::BN;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * G::BN;
-      if (p.tma_store) {
-        if (p.out_dtype == GEMM_BF16)
-          epilogue_tma<G::BN, GEMM_BF16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
-        else if (p.out_dtype == GEMM_F16)
-          epilogue_tma<G::BN, GEMM_F16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
-        else
-          epilogue_tma<G::BN, GEMM_F32>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+      // First row of this warp's 32 rows in worker w's partial tile (row-major, BN columns).
+      auto part_row0 = [&](int w) { return (w * 2 + static_cast<int>(rank)) * G::BM + quarter * 32; };
+      if (seg.role == kSegPartial) {
+        // Split-K piece that starts inside the tile: its fp32 sum goes to this worker's
+        // workspace entry by TMA store; the flag tells the tile's owner it is in memory.
+        epilogue_tma<G::BN, GEMM_F32>(&tmP, t_row, bufs, buf, lane, part_row0(cluster_id), 0,
+                                      INT32_MAX, G::BN);
+        if (lane == 0) {
+          bulk_wait_group<0>();  // the partial's writes are complete
+          fence_proxy_async_global();
+          st_release_gpu(p.sk_flags + (cluster_id * 2 + rank) * 4 + quarter, p.sk_epoch);
+        }
+        __syncwarp();
       } else {
-        if (p.out_dtype == GEMM_BF16)
-          epilogue_direct<G::BN, GEMM_BF16>(p, t_row, row0 + lane, n0);
-        else if (p.out_dtype == GEMM_F16)
-          epilogue_direct<G::BN, GEMM_F16>(p, t_row, row0 + lane, n0);
-        else
-          epilogue_direct<G::BN, GEMM_F32>(p, t_row, row0 + lane, n0);
+        if (seg.role == kSegOwner) {
+          // The rest of this tile was computed by workers first_src..last_src: add their
+          // partials into the accumulator in increasing worker order (a fixed order). The
+          // owner piece is its worker's last, so the pipeline stages are idle and each
+          // epilogue warp borrows a slice of them to receive a partial by TMA.
+          uint8_t *slice = smem + e * G::OWNER_SLICE;
+          for (int w = seg.first_src; ok && w <= seg.last_src; ++w) {
+            ok = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, p.sk_epoch, wd);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            fence_proxy_async_global();
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&part_bar[e], G::BN * 32 * 4);
+#pragma unroll
+              for (int b = 0; b < G::BN / 32; ++b)
+                tma_load_2d(smem_u32(slice + b * kStoreBufBytes), &tmP, smem_u32(&part_bar[e]),
+                            b * 32, part_row0(w));
+            }
+            ok = mbar_wait(&part_bar[e], part_phase, wd);
+            ok = __all_sync(0xffffffffu, ok);
+            part_phase ^= 1;
+            if (!ok) break;
+            add_partial_into_tmem<G::BN>(t_row, slice, lane);
+          }
+          if (!ok) break;
+        }
+        if (p.tma_store) {
+          if (p.out_dtype == GEMM_BF16)
+            epilogue_tma<G::BN, GEMM_BF16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+          else if (p.out_dtype == GEMM_F16)
+            epilogue_tma<G::BN, GEMM_F16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+          else
+            epilogue_tma<G::BN, GEMM_F32>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
+        } else {
+          if (p.out_dtype == GEMM_BF16)
+            epilogue_direct<G::BN, GEMM_BF16>(p, t_row, row0 + lane, n0);
+          else if (p.out_dtype == GEMM_F16)
+            epilogue_direct<G::BN, GEMM_F16>(p, t_row, row0 + lane, n0);
+          else
+            epilogue_direct<G::BN, GEMM_F32>(p, t_row, row0 + lane, n0);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -243,35 +300,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int ESIZE, bool A_MN, bool B_MN, int BN>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                        const TcParams &p, int grid, cudaStream_t s) {
+                        const CUtensorMap &tmP, const TcParams &p, int grid, cudaStream_t s) {
   using G = Cfg2<ESIZE, A_MN, B_MN, BN>;
   auto kernel = tc2_gemm_kernel<ESIZE, A_MN, B_MN, BN>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Split-K owners wait for partials of other clusters of the same launch: ask for all
+  // CTAs to be resident at once.
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  const bool split = p.sk_dp_tiles < p.tiles_m * p.tiles_n;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = G::SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, p);
+  cfg.numAttrs = split ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmP, p);
 }
 
 template <int ESIZE, int BN>
 cudaError_t launch_pair_majors(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                               const CUtensorMap &tmC, const TcParams &p, int grid,
-                               cudaStream_t s) {
-  if (!v.a_mn && !v.b_mn) return launch_pair<ESIZE, false, false, BN>(tmA, tmB, tmC, p, grid, s);
-  if (!v.a_mn && v.b_mn) return launch_pair<ESIZE, false, true, BN>(tmA, tmB, tmC, p, grid, s);
-  if (v.a_mn && !v.b_mn) return launch_pair<ESIZE, true, false, BN>(tmA, tmB, tmC, p, grid, s);
-  return launch_pair<ESIZE, true, true, BN>(tmA, tmB, tmC, p, grid, s);
+                               const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p,
+                               int grid, cudaStream_t s) {
+  if (!v.a_mn && !v.b_mn) return launch_pair<ESIZE, false, false, BN>(tmA, tmB, tmC, tmP, p, grid, s);
+  if (!v.a_mn && v.b_mn) return launch_pair<ESIZE, false, true, BN>(tmA, tmB, tmC, tmP, p, grid, s);
+  if (v.a_mn && !v.b_mn) return launch_pair<ESIZE, true, false, BN>(tmA, tmB, tmC, tmP, p, grid, s);
+  return launch_pair<ESIZE, true, true, BN>(tmA, tmB, tmC, tmP, p, grid, s);
 }
 
 }  // namespace
@@ -312,13 +374,16 @@ int tc2_max_active_clusters() {
 }
 
 cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                       const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
+                       const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p, int grid,
+                       cudaStream_t s) {
   // tf32 operands are always K-major (MN-major fp32 operands are staged transposed).
-  if (v.esize == 2 && v.block_n == 256) return launch_pair_majors<2, 256>(v, tmA, tmB, tmC, p, grid, s);
-  if (v.esize == 2 && v.block_n == 128) return launch_pair_majors<2, 128>(v, tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 2 && v.block_n == 256)
+    return launch_pair_majors<2, 256>(v, tmA, tmB, tmC, tmP, p, grid, s);
+  if (v.esize == 2 && v.block_n == 128)
+    return launch_pair_majors<2, 128>(v, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.esize == 4 && !v.a_mn && !v.b_mn) {
-    if (v.block_n == 256) return launch_pair<4, false, false, 256>(tmA, tmB, tmC, p, grid, s);
-    if (v.block_n == 128) return launch_pair<4, false, false, 128>(tmA, tmB, tmC, p, grid, s);
+    if (v.block_n == 256) return launch_pair<4, false, false, 256>(tmA, tmB, tmC, tmP, p, grid, s);
+    if (v.block_n == 128) return launch_pair<4, false, false, 128>(tmA, tmB, tmC, tmP, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -10,6 +10,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "sk_schedule.h"
 
 namespace gemm_gb300 {
 namespace tc {
@@ -133,6 +134,89 @@ __device__ __forceinline__ void epilogue_direct(const TcParams &p, uint32_t t_ro
     }
   }
 }
+
+// Split-K owner: adds one partial (this warp's 32 rows x BN fp32, already TMA-loaded into
+// `slice` as BN/32 128B-swizzled boxes of 32 rows x 32 columns) into its TMEM rows.
+template <int BN>
+__device__ __forceinline__ void add_partial_into_tmem(uint32_t t_row, const uint8_t *slice,
+                                                      int lane) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + c0, r);
+    tmem_wait_ld();
+    const uint32_t row_addr = smem_u32(slice + (c0 / 32) * kStoreBufBytes) + lane * kRowBytes;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float4 v;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                   : "r"(row_addr + ((ch ^ (lane & 7)) << 4)));
+      r[4 * ch + 0] = __float_as_uint(__uint_as_float(r[4 * ch + 0]) + v.x);
+      r[4 * ch + 1] = __float_as_uint(__uint_as_float(r[4 * ch + 1]) + v.y);
+      r[4 * ch + 2] = __float_as_uint(__uint_as_float(r[4 * ch + 2]) + v.z);
+      r[4 * ch + 3] = __float_as_uint(__uint_as_float(r[4 * ch + 3]) + v.w);
+    }
+    tmem_st_32x32b_x32(t_row + c0, r);
+  }
+  tmem_wait_st();
+}
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *flag == value (a split-K partial of this launch is in memory).
+__device__ __forceinline__ bool wait_flag(const int *flag, int value, const Watchdog &wd) {
+  if (ld_acquire_gpu(flag) == value) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(flag) != value) {
+    if (*wd.abort_flag) return false;
+    if (global_timer_ns() - t0 > wd.timeout_ns) {
+      atomicCAS(wd.status, 0, kStatusTimeout);
+      *wd.abort_flag = 1;
+      __threadfence_block();
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// The pieces of work of one persistent worker: its round-robin whole tiles, then its
+// split-K share (see sk_schedule.h). Every role of a worker walks the same sequence.
+struct WorkIter {
+  SkSchedule S;
+  int32_t slot, dp_i, dp_n;
+  int64_t u, hi;
+  __device__ __forceinline__ WorkIter(const SkSchedule &s, int32_t w) : S(s), slot(w), dp_i(0) {
+    dp_n = sk_dp_count(S, slot);
+    u = sk_begin(S, slot);
+    hi = sk_begin(S, slot + 1);
+  }
+  __device__ __forceinline__ bool next(SkSegment &seg) {
+    if (dp_i < dp_n) {
+      seg.tile = slot + dp_i * S.slots;
+      seg.kb_begin = 0;
+      seg.kb_end = S.kb;
+      seg.role = kSegFull;
+      seg.first_src = seg.last_src = -1;
+      ++dp_i;
+      return true;
+    }
+    if (u < hi) {
+      u = sk_segment_at(S, slot, u, &seg);
+      return true;
+    }
+    return false;
+  }
+};
 
 }  // namespace tc
 }  // namespace gemm_gb300

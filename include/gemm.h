@@ -149,8 +149,11 @@ typedef enum {
   GEMM_OPT_CTA_PAIR = 6,        /* tensor-core tiles: 0 auto, 1 single-CTA (128 rows),
                                    2 CTA-pair (256 rows, cta_group::2 on two SMs) */
   GEMM_OPT_BLOCK_N = 7,         /* tensor-core tile width: 0 auto, 128 or 256 */
-  GEMM_OPT_EXACT_CHUNK = 8      /* exact fp32: 32-long K-blocks summed in TMEM before each
+  GEMM_OPT_EXACT_CHUNK = 8,     /* exact fp32: 32-long K-blocks summed in TMEM before each
                                    fp32 register add (0 = by K: k_blocks/24 in [1, 16]; 1..64) */
+  GEMM_OPT_STREAM_K = 9         /* 0: split the last, partly filled rounds of tiles along K
+                                   (fixed-order reduction, handle-owned workspace); 1: whole
+                                   tiles only */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
@@ -182,7 +185,7 @@ typedef struct {
   int64_t ctas;           /* CTAs launched (persistent schedule; pairs count twice) */
   int64_t workspace_bytes; /* workspace the call needs */
   int32_t cta_pair;       /* 1 if tiles run on CTA pairs (two SMs per tile) */
-  int32_t reserved;
+  int32_t split_tiles;    /* tiles of the last rounds split along K (split-K) */
 } gemm_plan_info_t;
 
 /* Host-only: the plan gemm_run_ex would use for these arguments on a GPU with

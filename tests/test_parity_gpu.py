@@ -247,14 +247,21 @@ def test_misaligned_operands_are_staged(h):
 # ------------------------------------------------- schedule and determinism
 
 def test_schedule_options_do_not_change_bits(h):
+    # With whole tiles only, every output tile is the same K-loop whatever the raster order,
+    # grid size or staging: the bits cannot depend on the schedule. (Split-K changes the
+    # fp32 summation order of the split tiles; it is covered by its own tests.)
     import dense_tiled_gemm_05_gb300 as g
     p = W.bf16_square(1024)
     a, b = to_device(p.A), to_device(p.B)
-    base = h.matmul(a, b)
-    assert h.status() == 0
+    h0 = g.Gemm(0)
+    h0.set_option("stream_k", 1)
+    base = h0.matmul(a, b)
+    assert h0.status() == 0
+    h0.close()
     for opts in ({"max_ctas": 3}, {"group_m": 1}, {"group_m": 5, "max_ctas": 17},
                  {"force_staging": 1}):
         h2 = g.Gemm(0)
+        h2.set_option("stream_k", 1)
         for k, v in opts.items():
             h2.set_option(k, v)
         c = h2.matmul(a, b)
@@ -277,6 +284,51 @@ def test_mid_size_full_compare_many_tiles_per_cta(h, cta_pair, max_ctas):
         ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
         assert torch.equal(c.cpu().to(torch.int64), ref)
     h2.close()
+
+
+@pytest.mark.parametrize("M,N,K,max_ctas", [(2048, 2048, 2048, 0), (1500, 1300, 700, 10),
+                                            (600, 600, 1000, 16), (256, 256, 8192, 0),
+                                            (1030, 530, 1200, 8)])
+def test_split_k_integer_exact(h, M, N, K, max_ctas):
+    # Shapes whose last round of tiles is split along K: pieces of tiles are summed by
+    # their owners from fp32 partials in a fixed order. Integer inputs keep every partial
+    # exact, so the result must match the int64 product bit for bit. (256 x 256 x 8192 is
+    # a single tile shared by every cluster: one owner adds dozens of partials.)
+    import dense_tiled_gemm_05_gb300 as g
+    h2 = g.Gemm(0)
+    h2.set_option("cta_pair", 2)
+    h2.set_option("block_n", 256)
+    if max_ctas:
+        h2.set_option("max_ctas", max_ctas)
+    p = W.integer_problem(M, N, K, "bf16", seed=M + K, b_layout="col")
+    plan = h2.plan(to_device(p.A), to_device(p.B), out_dtype="f32")
+    assert plan["split_tiles"] > 0, plan
+    for _ in range(2):  # twice: the second launch reuses the workspace with a new epoch
+        c = run_gpu(h2, p)
+        assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    h2.close()
+
+
+def test_split_k_matches_whole_tiles_and_is_deterministic(h):
+    import dense_tiled_gemm_05_gb300 as g
+    p = W.bf16_square(4096)
+    a, b = to_device(p.A), to_device(p.B)
+    assert h.plan(a, b)["split_tiles"] > 0
+    c1 = h.matmul(a, b)
+    c2 = h.matmul(a, b)
+    assert h.status() == 0
+    assert torch.equal(c1, c2)  # fixed reduction order: bitwise repeatable
+    whole = g.Gemm(0)
+    whole.set_option("stream_k", 1)
+    assert whole.plan(a, b)["split_tiles"] == 0
+    c3 = whole.matmul(a, b)
+    assert whole.status() == 0
+    whole.close()
+    rows = list(range(0, 4096, 97))
+    C64, D = oracle_rows(p, rows)
+    assert rel_err(c1[rows], C64, D) <= 1e-2 and rel_err(c3[rows], C64, D) <= 1e-2
+    # the two schedules only differ in fp32 summation order before the bf16 rounding
+    assert float((c1.float() - c3.float()).abs().max()) <= 2 * 2.0 ** -8 * float(c3.float().abs().max())
 
 
 def test_deterministic(h):
