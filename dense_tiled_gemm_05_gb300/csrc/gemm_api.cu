@@ -243,20 +243,32 @@ OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, 
   return o;
 }
 
+// Whether splitting the last rounds along K pays on GB300 (interleaved measurements of
+// bf16 products): it does when at least two whole rounds come first and every tile has a
+// long K-loop (4096^3 +5.6 %, 5120^3 +7.4 %, 8192^3 +3.6 %); it does not when every tile
+// has to be split (2048^3 -26 %) or K is short (8192 x 8192 x 2048 -1.6 %), where the
+// partial-tile traffic costs more than the idle tail it saves. stream_k: 0 by this rule,
+// 1 never, 2 whenever the schedule allows.
+bool use_split_k(int stream_k, int64_t tiles, int64_t k_blocks, int64_t slots) {
+  if (stream_k == 1) return false;
+  if (stream_k == 2) return true;
+  return slots > 0 && tiles % slots != 0 && tiles / slots >= 2 && k_blocks >= 64;
+}
+
 // Tile width by a wave-quantisation cost model: a persistent grid runs
 // ceil(tiles / slots) rounds, each as long as one tile. A 128-wide tile has half the
 // flops of a 256-wide one but, measured on GB300, takes about 0.75 of its time (every MMA
 // re-reads its 128 x 16 slice of A from shared memory, so narrow MMAs are starved of
 // shared-memory bandwidth); it wins only when it fills the machine much better, e.g.
 // when N itself is at most 128.
-int pick_block_n(int64_t M, int64_t N, int64_t k_blocks, bool pair, bool stream_k, int sm_count) {
+int pick_block_n(int64_t M, int64_t N, int64_t k_blocks, bool pair, int stream_k, int sm_count) {
   const int64_t rows = pair ? 2 * kTcBlockM : kTcBlockM;
   const int64_t slots = pair ? (sm_count > 1 ? sm_count / 2 : 1) : (sm_count > 0 ? sm_count : 1);
   const int64_t tiles_m = (M + rows - 1) / rows;
   auto cost = [&](int64_t bn, double per_column) {
     const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
     // With a split-K share the last round is spread over every slot: fractional rounds.
-    const bool split = pair && stream_k &&
+    const bool split = pair && use_split_k(stream_k, tiles, k_blocks, slots) &&
                        sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(k_blocks),
                                    static_cast<int32_t>(slots), true) < tiles;
     const double rounds = split ? static_cast<double>(tiles) / static_cast<double>(slots)
@@ -320,7 +332,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   pl.variant.block_n =
       opt.block_n ? opt.block_n
                   : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
-                                 opt.stream_k == 0 && !split, sm_count);
+                                 split ? 1 : opt.stream_k, sm_count);
   if (split) {  // the exact-fp32 kernel has one shape: CTA pairs, 256 x 256 tiles
     pl.variant.exact = true;
     pl.variant.pair = true;
@@ -349,7 +361,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
     // With a split-K share every cluster takes part, even when there are fewer tiles.
     int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
     if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
-    const bool split = !pl.variant.exact && opt.stream_k == 0 &&
+    const bool split = !pl.variant.exact && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
                        sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(I.k_iters),
                                    static_cast<int32_t>(clusters), true) < tiles;
     I.ctas = 2 * (split || tiles > clusters ? clusters : tiles);
@@ -360,10 +372,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   }
   I.workspace_bytes = static_cast<int64_t>(cursor);
   I.cta_pair = pl.variant.pair ? 1 : 0;
-  if (pl.variant.pair && !pl.variant.exact && opt.stream_k == 0) {
+  if (pl.variant.pair && !pl.variant.exact) {
     const int32_t slots = static_cast<int32_t>(I.ctas / 2);
     const int32_t t = static_cast<int32_t>(tiles);
-    I.split_tiles = t - sk_dp_tiles(t, static_cast<int32_t>(I.k_iters), slots, true);
+    if (use_split_k(opt.stream_k, t, I.k_iters, slots))
+      I.split_tiles = t - sk_dp_tiles(t, static_cast<int32_t>(I.k_iters), slots, true);
   }
   *out = pl;
   return GEMM_OK;
@@ -457,6 +470,7 @@ cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t 
 // Split-K context of a launch: a workspace provider (null = split-K off).
 struct SplitK {
   gemm_handle_t h = nullptr;
+  int mode = 1;  // GEMM_OPT_STREAM_K value
 };
 
 gemm_status_t ensure_sk_workspace(gemm_handle_t h, size_t bytes, size_t flag_bytes,
@@ -536,7 +550,8 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   tp.sk_dp_tiles = tiles;
   if (pl.variant.pair && !pl.variant.exact && sk.h) {
     const int32_t slots = static_cast<int32_t>(grid / 2);
-    tp.sk_dp_tiles = sk_dp_tiles(tiles, tp.k_blocks, slots, true);
+    tp.sk_dp_tiles = sk_dp_tiles(tiles, tp.k_blocks, slots,
+                                 use_split_k(sk.mode, tiles, tp.k_blocks, slots));
     if (tp.sk_dp_tiles < tiles) {
       const size_t flag_bytes = static_cast<size_t>(slots) * 2 * 4 * sizeof(int);
       const size_t flag_region = (flag_bytes + 255) / 256 * 256;
@@ -598,7 +613,8 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
       b_ptr = dst, b_ld = o->staged_ld;
   }
   SplitK sk;
-  if (h->stream_k == 0) sk.h = h;
+  sk.h = h;
+  sk.mode = h->stream_k;
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
                  h->group_m, h->stall_producer ? kDebugStallProducer : 0, h->exact_chunk, sk, s);
   if (st != GEMM_OK) return st;
@@ -621,9 +637,9 @@ GEMM_API int32_t gemm_schedule_segments(int32_t tiles, int32_t k_blocks, int32_t
       sk_make(tiles, k_blocks, slots, sk_dp_tiles(tiles, k_blocks, slots, stream_k != 0));
   if (whole_tiles) *whole_tiles = sk_dp_count(S, slot);
   int32_t n = 0;
-  for (int64_t u = sk_begin(S, slot), hi = sk_begin(S, slot + 1); u < hi; ++n) {
+  for (int64_t lo = sk_begin(S, slot), hi = sk_begin(S, slot + 1); hi > lo; ++n) {
     SkSegment seg;
-    u = sk_segment_at(S, slot, u, &seg);
+    hi = sk_segment_at(S, slot, hi, &seg);
     if (out && n < max_out)
       out[n] = gemm_segment_t{seg.tile, seg.kb_begin, seg.kb_end, seg.role, seg.first_src,
                               seg.last_src};
@@ -716,7 +732,7 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
       h->cta_pair = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_STREAM_K:
-      if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
+      if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->stream_k = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_EXACT_CHUNK:

@@ -6,14 +6,16 @@
 // `dp_tiles` tiles go round-robin to the slots whole ("data-parallel" rounds). The
 // remaining tiles are cut into their (tile, K-block) units, and every slot takes one
 // contiguous, equal share of those units ("stream-K"), so the last round ends at the same
-// time on every slot. A slot's share is a run of segments: a segment that covers a whole
-// tile is stored as usual; a segment that starts inside a tile is a *partial*: its fp32
-// sum goes to the slot's workspace entry; the segment that holds a tile's first K-block
-// (K-block 0) but not all of it is the tile's *owner*: it adds the partials of the slots
-// that cover the rest of that tile, in increasing slot order, and stores the result.
-// Every slot has at most one partial segment (only its first segment can start inside a
-// tile), so workspace entries are indexed by slot. Owners run at the end of a share and
-// partial writers at the start, so with equal shares an owner rarely waits.
+// time on every slot. A slot walks its share from the end to the start, in segments of at
+// most one tile: a segment covering a whole tile is stored as usual; a segment that lacks
+// its tile's last K-block is a *partial*: its fp32 sum goes to the slot's workspace entry;
+// the segment that holds a tile's last K-block but not all of it is the tile's *owner*: it
+// adds the partials of the slots that cover the start of that tile, in increasing slot
+// order, and stores the result. Walking backwards makes a slot's partial its first
+// segment (written early) and its owner segment its last (waiting late), and an owner only
+// ever waits for slots with smaller numbers, which the GPU dispatches no later than the
+// owner itself: the waits cannot block each other. Every slot has at most one partial
+// segment, so workspace entries are indexed by slot.
 //
 // Pure integer arithmetic, shared by the host planner and the device kernels.
 #pragma once
@@ -44,7 +46,7 @@ struct SkSegment {
   int32_t kb_begin;   // first K-block
   int32_t kb_end;     // one past the last K-block
   int32_t role;       // kSegFull, kSegPartial or kSegOwner
-  int32_t first_src;  // owner: first slot whose partial it adds
+  int32_t first_src;  // owner: first slot whose partial it adds (all lower than the owner)
   int32_t last_src;   // owner: last slot whose partial it adds
 };
 
@@ -89,26 +91,27 @@ SK_HD int32_t sk_dp_count(const SkSchedule &S, int32_t s) {
   return S.dp_tiles / S.slots + (s < S.dp_tiles % S.slots ? 1 : 0);
 }
 
-// The stream-K segment of slot s that starts at unit u (inside s's share); returns the
-// unit just after it, where the slot's next segment starts.
+// The stream-K segment of slot s that ends at unit u (exclusive; inside s's share, walking
+// backwards from the share's end); returns the unit where it starts, i.e. where the slot's
+// next segment ends.
 SK_HD int64_t sk_segment_at(const SkSchedule &S, int32_t s, int64_t u, SkSegment *seg) {
-  const int64_t hi = sk_begin(S, s + 1);
-  const int64_t t = u / S.kb;  // stream-K tile number
-  const int64_t end = (t + 1) * S.kb < hi ? (t + 1) * S.kb : hi;
+  const int64_t lo = sk_begin(S, s);
+  const int64_t t = (u - 1) / S.kb;  // stream-K tile number
+  const int64_t begin = t * S.kb > lo ? t * S.kb : lo;
   seg->tile = static_cast<int32_t>(S.dp_tiles + t);
-  seg->kb_begin = static_cast<int32_t>(u - t * S.kb);
-  seg->kb_end = static_cast<int32_t>(end - t * S.kb);
+  seg->kb_begin = static_cast<int32_t>(begin - t * S.kb);
+  seg->kb_end = static_cast<int32_t>(u - t * S.kb);
   seg->first_src = seg->last_src = -1;
-  if (seg->kb_begin > 0) {
+  if (seg->kb_end < S.kb) {
     seg->role = kSegPartial;
-  } else if (seg->kb_end < S.kb) {
+  } else if (seg->kb_begin > 0) {
     seg->role = kSegOwner;
-    seg->first_src = s + 1;
-    seg->last_src = sk_slot_of_unit(S, (t + 1) * S.kb - 1);
+    seg->first_src = sk_slot_of_unit(S, t * S.kb);
+    seg->last_src = s - 1;
   } else {
     seg->role = kSegFull;
   }
-  return end;
+  return begin;
 }
 
 }  // namespace gemm_gb300

@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // First row of this warp's 32 rows in worker w's partial tile (row-major, BN columns).
       auto part_row0 = [&](int w) { return (w * 2 + static_cast<int>(rank)) * G::BM + quarter * 32; };
       if (seg.role == kSegPartial) {
-        // Split-K piece that starts inside the tile: its fp32 sum goes to this worker's
+        // Split-K piece without its tile's last K-block: its fp32 sum goes to this worker's
         // workspace entry by TMA store; the flag tells the tile's owner it is in memory.
         epilogue_tma<G::BN, GEMM_F32>(&tmP, t_row, bufs, buf, lane, part_row0(cluster_id), 0,
                                       INT32_MAX, G::BN);
@@ -231,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       } else {
         if (seg.role == kSegOwner) {
-          // The rest of this tile was computed by workers first_src..last_src: add their
-          // partials into the accumulator in increasing worker order (a fixed order). The
-          // owner piece is its worker's last, so the pipeline stages are idle and each
-          // epilogue warp borrows a slice of them to receive a partial by TMA.
+          // The start of this tile was computed by workers first_src..last_src (all numbered
+          // below this one): add their partials into the accumulator in increasing worker
+          // order (a fixed order). The owner piece is its worker's last, so the pipeline
+          // stages are idle and each epilogue warp borrows a slice of them for the TMA loads.
           uint8_t *slice = smem + e * G::OWNER_SLICE;
           for (int w = seg.first_src; ok && w <= seg.last_src; ++w) {
             ok = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, p.sk_epoch, wd);
@@ -307,22 +307,17 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // Split-K owners wait for partials of other clusters of the same launch: ask for all
-  // CTAs to be resident at once.
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
-  const bool split = p.sk_dp_tiles < p.tiles_m * p.tiles_n;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = G::SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = split ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmP, p);
 }
 

@@ -194,10 +194,10 @@ __device__ __forceinline__ bool wait_flag(const int *flag, int value, const Watc
 struct WorkIter {
   SkSchedule S;
   int32_t slot, dp_i, dp_n;
-  int64_t u, hi;
+  int64_t lo, hi;  // split-K units still to do: [lo, hi)
   __device__ __forceinline__ WorkIter(const SkSchedule &s, int32_t w) : S(s), slot(w), dp_i(0) {
     dp_n = sk_dp_count(S, slot);
-    u = sk_begin(S, slot);
+    lo = sk_begin(S, slot);
     hi = sk_begin(S, slot + 1);
   }
   __device__ __forceinline__ bool next(SkSegment &seg) {
@@ -210,8 +210,8 @@ struct WorkIter {
       ++dp_i;
       return true;
     }
-    if (u < hi) {
-      u = sk_segment_at(S, slot, u, &seg);
+    if (hi > lo) {  // the split-K share, walked from its end to its start
+      hi = sk_segment_at(S, slot, hi, &seg);
       return true;
     }
     return false;

@@ -151,9 +151,10 @@ typedef enum {
   GEMM_OPT_BLOCK_N = 7,         /* tensor-core tile width: 0 auto, 128 or 256 */
   GEMM_OPT_EXACT_CHUNK = 8,     /* exact fp32: 32-long K-blocks summed in TMEM before each
                                    fp32 register add (0 = by K: k_blocks/24 in [1, 16]; 1..64) */
-  GEMM_OPT_STREAM_K = 9         /* 0: split the last, partly filled rounds of tiles along K
-                                   (fixed-order reduction, handle-owned workspace); 1: whole
-                                   tiles only */
+  GEMM_OPT_STREAM_K = 9         /* split the last, partly filled rounds of tiles along K
+                                   (fixed-order reduction, handle-owned workspace):
+                                   0 when it pays (>= 2 whole rounds first, >= 64 K-blocks),
+                                   1 never, 2 whenever the schedule allows */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
@@ -204,7 +205,8 @@ typedef struct {
   int32_t kb_begin;  /* first K-block of the tile this piece computes */
   int32_t kb_end;    /* one past its last K-block */
   int32_t role;      /* 0 whole tile, 1 partial (fp32 sum to the workspace), 2 owner (adds
-                        the partials of workers first_src..last_src, then stores) */
+                        the partials of workers first_src..last_src, all numbered below
+                        the owner, then stores) */
   int32_t first_src, last_src;
 } gemm_segment_t;
 
@@ -212,9 +214,11 @@ typedef struct {
  * `k_blocks` K-blocks each on `slots` persistent workers. With stream_k == 0 every tile is
  * done whole, round-robin. Otherwise the tiles of the last, partly filled rounds are cut
  * into K-blocks and shared equally (split-K with a fixed-order reduction: every partial is
- * added by the owner of its tile in increasing worker order). Writes worker `slot`'s
- * round-robin tile count to *whole_tiles and up to max_out of its split pieces to out;
- * returns the number of split pieces, or -1 for invalid arguments. */
+ * added by the owner of its tile in increasing worker order). A worker walks its share
+ * backwards, so its partial comes first and its owner piece last. Writes worker `slot`'s
+ * round-robin tile count to *whole_tiles and up to max_out of its split pieces, in the
+ * order the worker computes them, to out; returns the number of split pieces, or -1 for
+ * invalid arguments. */
 GEMM_API int32_t gemm_schedule_segments(int32_t tiles, int32_t k_blocks, int32_t slots,
                                         int32_t stream_k, int32_t slot, int32_t *whole_tiles,
                                         gemm_segment_t *out, int32_t max_out);

@@ -81,6 +81,7 @@ def test_plan_bf16_square_is_tcgen05_k_major():
     assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
     assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["tma_store"] == 1
     assert p["ctas"] == 148 and p["workspace_bytes"] == 0 and p["stages"] == 6
+    assert p["split_tiles"] == 108  # last rounds split along K (3.46 rounds of tiles)
     p = g.plan(t((8192, 8192), torch.bfloat16), t((8192, 8192), torch.bfloat16, "col"),
                sm_count=148)
     assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 256, 32, 32)

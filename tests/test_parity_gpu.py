@@ -298,6 +298,7 @@ def test_split_k_integer_exact(h, M, N, K, max_ctas):
     h2 = g.Gemm(0)
     h2.set_option("cta_pair", 2)
     h2.set_option("block_n", 256)
+    h2.set_option("stream_k", 2)  # split whenever the schedule allows, even for small shapes
     if max_ctas:
         h2.set_option("max_ctas", max_ctas)
     p = W.integer_problem(M, N, K, "bf16", seed=M + K, b_layout="col")

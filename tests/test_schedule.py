@@ -39,25 +39,28 @@ def check(tiles, kb, slots, stream_k=True):
             for k in range(b, e):
                 assert (t, k) not in covered, (t, k)
                 covered[(t, k)] = s
+            if i > 0:  # walked backwards: each piece ends where the previous one began
+                assert (t, e) == (segs[i - 1][0], kb) or (t == segs[i - 1][0] - 1 and e == kb)
             if role == PARTIAL:
-                assert b > 0 and i == 0, "only a share's first piece starts inside a tile"
+                assert e < kb and i == 0, "only a share's first piece lacks its tile's end"
                 partial_of[s] = t
             elif role == OWNER:
-                assert b == 0 and e < kb and i == len(segs) - 1
-                owners[t] = (s, f, l, e)
+                assert b > 0 and e == kb and i == len(segs) - 1
+                owners[t] = (s, f, l, b)
             else:
                 assert b == 0 and e == kb and f == l == -1
         work.append(units + whole * kb)
     assert len(covered) == tiles * kb
-    # every partial is gathered by the owner of its tile, in increasing worker order
+    # every partial is gathered by the owner of its tile, in increasing worker order, and an
+    # owner only waits for workers numbered below it
     gathered = set()
-    for t, (s, f, l, e) in owners.items():
-        assert f == s + 1 and l >= f
+    for t, (s, f, l, b) in owners.items():
+        assert l == s - 1 and f <= l
         for src in range(f, l + 1):
             assert partial_of.get(src) == t
             gathered.add(src)
-        # the sources cover exactly the rest of the tile
-        assert all(covered[(t, k)] in range(f, l + 1) for k in range(e, kb))
+        # the sources cover exactly the start of the tile
+        assert all(covered[(t, k)] in range(f, l + 1) for k in range(0, b))
     assert gathered == set(partial_of)
     if stream_k and tiles % slots and tiles * kb >= slots:
         assert max(work) - min(work) <= kb + 1  # the split share is balanced to a unit
