@@ -41,7 +41,7 @@ _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
-           "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments")
+           "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments", "gemm_run_host")
 
 
 class GemmError(RuntimeError):
@@ -92,6 +92,8 @@ def lib():
                 L.gemm_run.restype = i32
                 L.gemm_run_ex.argtypes = run_args + [i32, i32, vp]
                 L.gemm_run_ex.restype = i32
+                L.gemm_run_host.argtypes = run_args + [i32, i32, vp]
+                L.gemm_run_host.restype = i32
                 L.gemm_get_status.argtypes = [vp, vp]
                 L.gemm_get_status.restype = i32
                 L.gemm_strerror.argtypes = [i32]
@@ -221,6 +223,37 @@ class Gemm:
         _check(code, "gemm_run_ex")
         return out
 
+    def matmul_host(self, a, b, out=None, out_dtype=None, precision="default", stream=None):
+        """C = a @ b for HOST tensors through gemm_run_host: the library copies A and B to the
+        GPU and C back, overlapping the copies of one row panel with the product of another.
+
+        Pinned host tensors (``pin_memory=True``) give asynchronous copies; the call returns
+        once the work is enqueued on the stream, so synchronise before reading ``out``.
+        """
+        if a.is_cuda or b.is_cuda:
+            raise ValueError("matmul_host takes host tensors")
+        if a.dtype != b.dtype:
+            raise TypeError("a and b must share a dtype")
+        M, K = a.shape
+        K2, N = b.shape
+        if K != K2:
+            raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+        if out is None:
+            od = _TORCH_OF[_dtype_code(out_dtype)] if out_dtype is not None else a.dtype
+            out = torch.empty((M, N), dtype=od, pin_memory=True)
+        if out.is_cuda or out.dim() != 2 or out.shape != (M, N) or (N > 1 and out.stride(1) != 1):
+            raise ValueError("out must be a row-major M x N host tensor")
+        al, lda = operand_layout(a)
+        bl, ldb = operand_layout(b)
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        code = lib().gemm_run_host(self._h, M, N, K, ctypes.c_void_p(a.data_ptr()), lda,
+                                   ctypes.c_void_p(b.data_ptr()), ldb,
+                                   ctypes.c_void_p(out.data_ptr()), max(out.stride(0), N, 1),
+                                   _dtype_code(a.dtype), _dtype_code(out.dtype), PREC[precision],
+                                   al, bl, ctypes.c_void_p(s.cuda_stream))
+        _check(code, "gemm_run_host")
+        return out
+
     def plan(self, a, b, out=None, out_dtype=None, precision="default", sm_count=None):
         """The planner's decision for these operands (host-only, nothing launched)."""
         return plan(a, b, out=out, out_dtype=out_dtype, precision=precision,
@@ -271,29 +304,11 @@ def matmul(a, b, out=None, out_dtype=None, precision="default"):
     return handle(a.device.index).matmul(a, b, out=out, out_dtype=out_dtype, precision=precision)
 
 
-def matmul_host(a, b, out=None, out_dtype=None, precision="default", device=None, work=None):
-    """End-to-end product of HOST tensors: copy a and b to the GPU, multiply, copy C back.
-
-    ``work`` may hold preallocated device tensors {"a", "b", "c"} to reuse.
-    Host tensors should be pinned for asynchronous copies.
-    """
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    if work is None:
-        work = {}
-    da = work.get("a")
-    if da is None:
-        da = torch.empty_strided(a.shape, a.stride(), dtype=a.dtype, device=dev)
-    db = work.get("b")
-    if db is None:
-        db = torch.empty_strided(b.shape, b.stride(), dtype=b.dtype, device=dev)
-    da.copy_(a, non_blocking=True)
-    db.copy_(b, non_blocking=True)
-    dc = handle(dev.index).matmul(da, db, out=work.get("c"), out_dtype=out_dtype,
-                                  precision=precision)
-    if out is None:
-        out = torch.empty(dc.shape, dtype=dc.dtype, pin_memory=True)
-    out.copy_(dc, non_blocking=True)
-    return out
+def matmul_host(a, b, out=None, out_dtype=None, precision="default", device=None):
+    """End-to-end product of host tensors with the default handle of ``device`` (default:
+    the current device); see :meth:`Gemm.matmul_host`."""
+    dev = torch.cuda.current_device() if device is None else int(device)
+    return handle(dev).matmul_host(a, b, out=out, out_dtype=out_dtype, precision=precision)
 
 
 class Segment(ctypes.Structure):

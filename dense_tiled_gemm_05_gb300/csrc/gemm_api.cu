@@ -44,6 +44,13 @@ struct gemm_handle_s {
   void *sk_ws = nullptr;
   size_t sk_ws_bytes = 0;
   int32_t sk_epoch = 0;
+  // host-buffer pipeline (gemm_run_host): device copies of A, B, C, streams and events
+  static constexpr int kMaxPanels = 8;
+  void *hp_buf = nullptr;
+  size_t hp_bytes = 0;
+  cudaStream_t hp_stream[3] = {nullptr, nullptr, nullptr};  // H2D, compute, D2H
+  cudaEvent_t hp_event[3 + 2 * kMaxPanels] = {};
+  bool hp_ready = false;
 };
 
 namespace {
@@ -696,6 +703,11 @@ GEMM_API void gemm_destroy(gemm_handle_t h) {
   cudaDeviceSynchronize();
   if (h->workspace) cudaFree(h->workspace);
   if (h->sk_ws) cudaFree(h->sk_ws);
+  if (h->hp_buf) cudaFree(h->hp_buf);
+  if (h->hp_ready) {
+    for (cudaStream_t st : h->hp_stream) cudaStreamDestroy(st);
+    for (cudaEvent_t ev : h->hp_event) cudaEventDestroy(ev);
+  }
   if (h->status) cudaFree(h->status);
   delete h;
 }
@@ -790,6 +802,127 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
                                 gemm_precision_t precision_mode) {
   return gemm_run_ex(h, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode,
                      GEMM_ROW_MAJOR, GEMM_ROW_MAJOR, nullptr);
+}
+
+namespace {
+
+// 2D copy of `rows` lines of `width` bytes between pitched buffers.
+cudaError_t copy2d(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width,
+                   size_t rows, cudaMemcpyKind kind, cudaStream_t s) {
+  if (rows == 0 || width == 0) return cudaSuccess;
+  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
+}
+
+gemm_status_t host_pipeline_setup(gemm_handle_t h) {
+  if (h->hp_ready) return GEMM_OK;
+  for (cudaStream_t &st : h->hp_stream)
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
+  for (cudaEvent_t &ev : h->hp_event)
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return GEMM_ERR_CUDA;
+  h->hp_ready = true;
+  return GEMM_OK;
+}
+
+}  // namespace
+
+GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                     const void *A, int64_t lda, const void *B, int64_t ldb,
+                                     void *C, int64_t ldc, gemm_dtype_t in_dtype,
+                                     gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
+                                     gemm_layout_t a_layout, gemm_layout_t b_layout,
+                                     void *cuda_stream) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  const Problem HP{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
+                   b_layout};
+  gemm_status_t st = check_args(HP);
+  if (st != GEMM_OK) return st;
+  DeviceGuard g(h->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaStream_t user = static_cast<cudaStream_t>(cuda_stream);
+  if (M == 0 || N == 0) return GEMM_OK;
+  const int es = esize_of(in_dtype), os = esize_of(out_dtype);
+  const int64_t align_e = 16 / es, align_o = 16 / os;
+  // Device copies with 16-byte aligned leading dimensions (TMA-legal in place).
+  const bool a_row = a_layout == GEMM_ROW_MAJOR, b_row = b_layout == GEMM_ROW_MAJOR;
+  const int64_t a_outer = a_row ? M : K, a_inner = a_row ? K : M;
+  const int64_t b_outer = b_row ? K : N, b_inner = b_row ? N : K;
+  const int64_t lda_d = round_up(a_inner > 0 ? a_inner : 1, align_e);
+  const int64_t ldb_d = round_up(b_inner > 0 ? b_inner : 1, align_e);
+  const int64_t ldc_d = round_up(N, align_o);
+  const size_t a_bytes = static_cast<size_t>(round_up(a_outer * lda_d * es, 256));
+  const size_t b_bytes = static_cast<size_t>(round_up(b_outer * ldb_d * es, 256));
+  const size_t c_bytes = static_cast<size_t>(M * ldc_d * os);
+  st = host_pipeline_setup(h);
+  if (st != GEMM_OK) return st;
+  if (a_bytes + b_bytes + c_bytes > h->hp_bytes) {
+    // earlier calls may still copy from or into the old buffer
+    for (cudaStream_t hs : h->hp_stream) cudaStreamSynchronize(hs);
+    if (h->hp_buf) cudaFree(h->hp_buf);
+    h->hp_buf = nullptr;
+    h->hp_bytes = 0;
+    if (cudaMalloc(&h->hp_buf, a_bytes + b_bytes + c_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_MEMORY;
+    }
+    h->hp_bytes = a_bytes + b_bytes + c_bytes;
+  }
+  char *dA = static_cast<char *>(h->hp_buf);
+  char *dB = dA + a_bytes;
+  char *dC = dB + b_bytes;
+  // Row panels of A (and of C): copies of panel i+1 and of C panel i-1 overlap the GEMM of
+  // panel i. Panels of at least 2048 rows (a multiple of the 256-row CTA-pair tile).
+  int panels = static_cast<int>(M / 2048);
+  panels = panels < 1 ? 1 : panels > gemm_handle_s::kMaxPanels / 2 ? gemm_handle_s::kMaxPanels / 2
+                                                                    : panels;
+  const int64_t panel_rows = round_up((M + panels - 1) / panels, 256);
+  cudaStream_t s_in = h->hp_stream[0], s_mm = h->hp_stream[1], s_out = h->hp_stream[2];
+  cudaEvent_t e_start = h->hp_event[0], e_b = h->hp_event[1], e_done = h->hp_event[2];
+  cudaEvent_t *e_a = h->hp_event + 3, *e_g = h->hp_event + 3 + gemm_handle_s::kMaxPanels;
+  cudaError_t e = cudaEventRecord(e_start, user);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, e_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_mm, e_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, e_start, 0);
+  if (e == cudaSuccess && K > 0)
+    e = copy2d(dB, ldb_d * es, B, ldb * es, b_inner * es, b_outer, cudaMemcpyHostToDevice, s_in);
+  if (e == cudaSuccess) e = cudaEventRecord(e_b, s_in);
+  if (e != cudaSuccess) return cuda_fail(e, "host pipeline: B");
+  int p = 0;
+  for (int64_t r0 = 0; r0 < M; r0 += panel_rows, ++p) {
+    const int64_t rows = M - r0 < panel_rows ? M - r0 : panel_rows;
+    // A panel rows [r0, r0 + rows)
+    if (K > 0) {
+      if (a_row)
+        e = copy2d(dA + r0 * lda_d * es, lda_d * es,
+                   static_cast<const char *>(A) + r0 * lda * es, lda * es, K * es, rows,
+                   cudaMemcpyHostToDevice, s_in);
+      else
+        e = copy2d(dA + r0 * es, lda_d * es, static_cast<const char *>(A) + r0 * es, lda * es,
+                   rows * es, K, cudaMemcpyHostToDevice, s_in);
+      if (e != cudaSuccess) return cuda_fail(e, "host pipeline: A");
+    }
+    if ((e = cudaEventRecord(e_a[p], s_in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s_mm, e_b, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s_mm, e_a[p], 0)) != cudaSuccess)
+      return cuda_fail(e, "host pipeline: order");
+    const void *a_panel = a_row ? static_cast<const void *>(dA + r0 * lda_d * es)
+                                : static_cast<const void *>(dA + r0 * es);
+    const Problem P{rows, N, K, a_panel, lda_d, dB, ldb_d, dC + r0 * ldc_d * os, ldc_d,
+                    in_dtype, out_dtype, precision_mode, a_layout, b_layout};
+    Plan pl;
+    st = make_plan(P, options_of(h), h->sm_count, &pl);
+    if (st != GEMM_OK) return st;
+    st = execute(h, P, pl, s_mm);
+    if (st != GEMM_OK) return st;
+    if ((e = cudaEventRecord(e_g[p], s_mm)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s_out, e_g[p], 0)) != cudaSuccess ||
+        (e = copy2d(static_cast<char *>(C) + r0 * ldc * os, ldc * os, dC + r0 * ldc_d * os,
+                    ldc_d * os, N * os, rows, cudaMemcpyDeviceToHost, s_out)) != cudaSuccess)
+      return cuda_fail(e, "host pipeline: C");
+  }
+  if ((e = cudaEventRecord(e_done, s_out)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(user, e_done, 0)) != cudaSuccess)
+    return cuda_fail(e, "host pipeline: join");
+  return GEMM_OK;
 }
 
 GEMM_API gemm_status_t gemm_get_status(gemm_handle_t h, void *cuda_stream) {

@@ -126,6 +126,22 @@ GEMM_API gemm_status_t gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_
                                    gemm_layout_t a_layout, gemm_layout_t b_layout,
                                    void *cuda_stream);
 
+/* C = A @ B for operands in HOST memory (A, B, C are host pointers; pinned memory makes
+ * the copies asynchronous and fast, pageable memory works but copies synchronously).
+ * Same arguments, layouts and checks as gemm_run_ex. The handle copies B to the device,
+ * streams A in row panels and C back out in row panels on its own streams, so that the
+ * copies of one panel overlap the product of another; the work starts after everything
+ * enqueued on `cuda_stream` before the call, and `cuda_stream` waits for its end (C is
+ * complete in host memory once that stream reaches this point). The device copies live in
+ * a handle-owned buffer that grows on demand. Device-side faults are reported by
+ * gemm_get_status. */
+GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                     const void *A, int64_t lda, const void *B, int64_t ldb,
+                                     void *C, int64_t ldc, gemm_dtype_t in_dtype,
+                                     gemm_dtype_t out_dtype, gemm_precision_t precision_mode,
+                                     gemm_layout_t a_layout, gemm_layout_t b_layout,
+                                     void *cuda_stream);
+
 /* Synchronise `cuda_stream` (NULL = legacy default stream), then read and clear
  * the handle's device status word. Returns GEMM_OK, GEMM_ERR_TIMEOUT when a
  * kernel's bounded wait expired since the last call (its C is then

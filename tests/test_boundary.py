@@ -54,6 +54,7 @@ def test_create_without_gpu_reports_device_error(L):
 def test_null_handle_is_rejected(L):
     assert L.gemm_run(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0) == 1
     assert L.gemm_get_status(None, None) == 1
+    assert L.gemm_run_host(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0, 0, 0, None) == 1
     assert L.gemm_set_option(None, 0, 1) == 1
     L.gemm_destroy(None)  # no-op
 
