@@ -359,7 +359,7 @@ def main():
         ha.copy_(p.A)
         hb.copy_(p.B)
         hc = torch.empty((p.M, p.N), dtype=out_dt, pin_memory=True)
-        for _ in range(3):
+        for _ in range(10):
             h.matmul_host(ha, hb, out=hc, precision=p.precision)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -40,16 +40,17 @@ struct gemm_handle_s {
   int block_n = 0;   // 0 auto, else 128 or 256
   int exact_chunk = 0;  // 0 default
   int stream_k = 0;     // 0 auto (on), 1 off
+  int host_panel = 0;  // gemm_run_host panel width (rows of A, columns of B), 0 auto
   // split-K workspace of the CTA-pair kernel: partial tiles and flags
   void *sk_ws = nullptr;
   size_t sk_ws_bytes = 0;
   int32_t sk_epoch = 0;
   // host-buffer pipeline (gemm_run_host): device copies of A, B, C, streams and events
-  static constexpr int kMaxPanels = 8;
+  static constexpr int kMaxPanels = 48;  // per operand; steps <= 2 * kMaxPanels
   void *hp_buf = nullptr;
   size_t hp_bytes = 0;
   cudaStream_t hp_stream[3] = {nullptr, nullptr, nullptr};  // H2D, compute, D2H
-  cudaEvent_t hp_event[3 + 2 * kMaxPanels] = {};
+  cudaEvent_t hp_event[2 + 4 * kMaxPanels] = {};
   bool hp_ready = false;
 };
 
@@ -743,6 +744,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
       return GEMM_OK;
+    case GEMM_OPT_HOST_PANEL:
+      if (v < 0 || v > (int64_t{1} << 30) || v % 256) return GEMM_ERR_INVALID_ARG;
+      h->host_panel = static_cast<int>(v);
+      return GEMM_OK;
     case GEMM_OPT_STREAM_K:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->stream_k = static_cast<int>(v);
@@ -813,6 +818,27 @@ cudaError_t copy2d(void *dst, size_t dpitch, const void *src, size_t spitch, siz
   return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
 }
 
+// Splits [0, extent) into copy panels, writing their starts and the end to start[] and
+// returning their number: panels of width w (`width`, else about extent/6, at least 1024; a
+// multiple of 256, the CTA-pair tile) while more than two remain, then halves down to 256, so
+// that the last product and the last copy out, which nothing overlaps, are short.
+int host_panels(int64_t extent, int64_t width, int64_t *start) {
+  constexpr int kMax = gemm_handle_s::kMaxPanels;
+  int64_t w = width;
+  if (w == 0) w = round_up((extent + 5) / 6, 256) < 1024 ? 1024 : round_up((extent + 5) / 6, 256);
+  if ((extent + w - 1) / w > kMax / 2) w = round_up((extent + kMax / 2 - 1) / (kMax / 2), 256);
+  int n = 0;
+  for (int64_t x = 0; x < extent; ++n) {
+    const int64_t left = extent - x;
+    int64_t len = left > 2 * w ? w : left <= 256 ? left : round_up(left / 2, 256);
+    if (n == kMax - 1) len = left;
+    start[n] = x;
+    x += len;
+  }
+  start[n] = extent;
+  return n;
+}
+
 gemm_status_t host_pipeline_setup(gemm_handle_t h) {
   if (h->hp_ready) return GEMM_OK;
   for (cudaStream_t &st : h->hp_stream)
@@ -869,55 +895,71 @@ GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int6
   char *dA = static_cast<char *>(h->hp_buf);
   char *dB = dA + a_bytes;
   char *dC = dB + b_bytes;
-  // Row panels of A (and of C): copies of panel i+1 and of C panel i-1 overlap the GEMM of
-  // panel i. Panels of at least 2048 rows (a multiple of the 256-row CTA-pair tile).
-  int panels = static_cast<int>(M / 2048);
-  panels = panels < 1 ? 1 : panels > gemm_handle_s::kMaxPanels / 2 ? gemm_handle_s::kMaxPanels / 2
-                                                                    : panels;
-  const int64_t panel_rows = round_up((M + panels - 1) / panels, 256);
+  const char *hA = static_cast<const char *>(A), *hB = static_cast<const char *>(B);
+  char *hC = static_cast<char *>(C);
+
+  // The copies in alternate between row panels of A and column panels of B (A first). Each
+  // arriving panel completes the C block that pairs it with every panel of the other operand
+  // already on the device; that block is multiplied (one product over the full K) and copied
+  // out while later panels copy in, so the copy out starts after two panels instead of after
+  // all of B.
+  int64_t a_start[gemm_handle_s::kMaxPanels + 1], b_start[gemm_handle_s::kMaxPanels + 1];
+  const int na = host_panels(M, h->host_panel, a_start);
+  const int nb = host_panels(N, h->host_panel, b_start);
   cudaStream_t s_in = h->hp_stream[0], s_mm = h->hp_stream[1], s_out = h->hp_stream[2];
-  cudaEvent_t e_start = h->hp_event[0], e_b = h->hp_event[1], e_done = h->hp_event[2];
-  cudaEvent_t *e_a = h->hp_event + 3, *e_g = h->hp_event + 3 + gemm_handle_s::kMaxPanels;
+  cudaEvent_t e_start = h->hp_event[0], e_done = h->hp_event[1];
+  cudaEvent_t *e_in = h->hp_event + 2, *e_mm = h->hp_event + 2 + 2 * gemm_handle_s::kMaxPanels;
   cudaError_t e = cudaEventRecord(e_start, user);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, e_start, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_mm, e_start, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, e_start, 0);
-  if (e == cudaSuccess && K > 0)
-    e = copy2d(dB, ldb_d * es, B, ldb * es, b_inner * es, b_outer, cudaMemcpyHostToDevice, s_in);
-  if (e == cudaSuccess) e = cudaEventRecord(e_b, s_in);
-  if (e != cudaSuccess) return cuda_fail(e, "host pipeline: B");
-  int p = 0;
-  for (int64_t r0 = 0; r0 < M; r0 += panel_rows, ++p) {
-    const int64_t rows = M - r0 < panel_rows ? M - r0 : panel_rows;
-    // A panel rows [r0, r0 + rows)
-    if (K > 0) {
-      if (a_row)
-        e = copy2d(dA + r0 * lda_d * es, lda_d * es,
-                   static_cast<const char *>(A) + r0 * lda * es, lda * es, K * es, rows,
-                   cudaMemcpyHostToDevice, s_in);
-      else
-        e = copy2d(dA + r0 * es, lda_d * es, static_cast<const char *>(A) + r0 * es, lda * es,
-                   rows * es, K, cudaMemcpyHostToDevice, s_in);
-      if (e != cudaSuccess) return cuda_fail(e, "host pipeline: A");
+  for (cudaStream_t hs : h->hp_stream)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs, e_start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "host pipeline: start");
+  int ia = 0, ib = 0;  // panels of A and of B on the device
+  for (int step = 0; ia < na || ib < nb; ++step) {
+    const bool take_a = ia < na && (ib >= nb || ia <= ib);
+    int64_t r0, rows, c0, cols;  // the C block this panel completes
+    if (take_a) {
+      r0 = a_start[ia];
+      rows = a_start[ia + 1] - r0;
+      c0 = 0;
+      cols = b_start[ib];
+      if (K > 0)
+        e = a_row ? copy2d(dA + r0 * lda_d * es, lda_d * es, hA + r0 * lda * es, lda * es, K * es,
+                           rows, cudaMemcpyHostToDevice, s_in)
+                  : copy2d(dA + r0 * es, lda_d * es, hA + r0 * es, lda * es, rows * es, K,
+                           cudaMemcpyHostToDevice, s_in);
+      ++ia;
+    } else {
+      c0 = b_start[ib];
+      cols = b_start[ib + 1] - c0;
+      r0 = 0;
+      rows = a_start[ia];
+      if (K > 0)
+        e = b_row ? copy2d(dB + c0 * es, ldb_d * es, hB + c0 * es, ldb * es, cols * es, K,
+                           cudaMemcpyHostToDevice, s_in)
+                  : copy2d(dB + c0 * ldb_d * es, ldb_d * es, hB + c0 * ldb * es, ldb * es,
+                           K * es, cols, cudaMemcpyHostToDevice, s_in);
+      ++ib;
     }
-    if ((e = cudaEventRecord(e_a[p], s_in)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s_mm, e_b, 0)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s_mm, e_a[p], 0)) != cudaSuccess)
+    if (e != cudaSuccess) return cuda_fail(e, "host pipeline: copy in");
+    if (rows == 0 || cols == 0) continue;  // nothing of the other operand yet
+    if ((e = cudaEventRecord(e_in[step], s_in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s_mm, e_in[step], 0)) != cudaSuccess)
       return cuda_fail(e, "host pipeline: order");
-    const void *a_panel = a_row ? static_cast<const void *>(dA + r0 * lda_d * es)
-                                : static_cast<const void *>(dA + r0 * es);
-    const Problem P{rows, N, K, a_panel, lda_d, dB, ldb_d, dC + r0 * ldc_d * os, ldc_d,
+    const char *a_blk = a_row ? dA + r0 * lda_d * es : dA + r0 * es;
+    const char *b_blk = b_row ? dB + c0 * es : dB + c0 * ldb_d * es;
+    char *c_blk = dC + (r0 * ldc_d + c0) * os;
+    const Problem P{rows, cols, K, a_blk, lda_d, b_blk, ldb_d, c_blk, ldc_d,
                     in_dtype, out_dtype, precision_mode, a_layout, b_layout};
     Plan pl;
     st = make_plan(P, options_of(h), h->sm_count, &pl);
     if (st != GEMM_OK) return st;
     st = execute(h, P, pl, s_mm);
     if (st != GEMM_OK) return st;
-    if ((e = cudaEventRecord(e_g[p], s_mm)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s_out, e_g[p], 0)) != cudaSuccess ||
-        (e = copy2d(static_cast<char *>(C) + r0 * ldc * os, ldc * os, dC + r0 * ldc_d * os,
-                    ldc_d * os, N * os, rows, cudaMemcpyDeviceToHost, s_out)) != cudaSuccess)
-      return cuda_fail(e, "host pipeline: C");
+    if ((e = cudaEventRecord(e_mm[step], s_mm)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s_out, e_mm[step], 0)) != cudaSuccess ||
+        (e = copy2d(hC + (r0 * ldc + c0) * os, ldc * os, c_blk, ldc_d * os, cols * os, rows,
+                    cudaMemcpyDeviceToHost, s_out)) != cudaSuccess)
+      return cuda_fail(e, "host pipeline: copy out");
   }
   if ((e = cudaEventRecord(e_done, s_out)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(user, e_done, 0)) != cudaSuccess)

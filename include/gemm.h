@@ -128,12 +128,14 @@ GEMM_API gemm_status_t gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_
 
 /* C = A @ B for operands in HOST memory (A, B, C are host pointers; pinned memory makes
  * the copies asynchronous and fast, pageable memory works but copies synchronously).
- * Same arguments, layouts and checks as gemm_run_ex. The handle copies B to the device,
- * streams A in row panels and C back out in row panels on its own streams, so that the
- * copies of one panel overlap the product of another; the work starts after everything
- * enqueued on `cuda_stream` before the call, and `cuda_stream` waits for its end (C is
- * complete in host memory once that stream reaches this point). The device copies live in
- * a handle-owned buffer that grows on demand. Device-side faults are reported by
+ * Same arguments, layouts and checks as gemm_run_ex. The handle copies row panels of A and
+ * column panels of B to the device in turn on its own streams; each arriving panel
+ * completes a block of C (its rows or columns against every panel of the other operand
+ * already there), which is multiplied and copied back while later panels copy in. The work
+ * starts after everything enqueued on `cuda_stream` before the call, and `cuda_stream`
+ * waits for its end (C is complete in host memory once that stream reaches this point).
+ * The device copies live in a handle-owned buffer that grows on demand (growing it waits
+ * for the handle's earlier host-path calls). Device-side faults are reported by
  * gemm_get_status. */
 GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                                      const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -167,10 +169,14 @@ typedef enum {
   GEMM_OPT_BLOCK_N = 7,         /* tensor-core tile width: 0 auto, 128 or 256 */
   GEMM_OPT_EXACT_CHUNK = 8,     /* exact fp32: 32-long K-blocks summed in TMEM before each
                                    fp32 register add (0 = by K: k_blocks/24 in [1, 16]; 1..64) */
-  GEMM_OPT_STREAM_K = 9         /* split the last, partly filled rounds of tiles along K
+  GEMM_OPT_STREAM_K = 9,        /* split the last, partly filled rounds of tiles along K
                                    (fixed-order reduction, handle-owned workspace):
                                    0 when it pays (>= 2 whole rounds first, >= 64 K-blocks),
                                    1 never, 2 whenever the schedule allows */
+  GEMM_OPT_HOST_PANEL = 10      /* gemm_run_host: rows of A and columns of B per pipelined
+                                   copy panel, a multiple of 256 (0 = auto: about 1/6 of the
+                                   extent, >= 1024; widened to keep <= 24 such panels); the
+                                   last two panels' worth is cut in halves down to 256 */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */

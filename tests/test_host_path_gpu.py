@@ -1,6 +1,6 @@
 """gemm_run_host: the product of operands held in host memory, with the copies to and
-from the device pipelined against the product inside the library (row panels of A and C
-on the handle's own streams). Compared with the exact product (integer inputs) and with
+from the device pipelined against the product inside the library (row panels of A and
+column panels of B in, blocks of C out, on the handle's own streams). Compared with the exact product (integer inputs) and with
 the oracle, for single- and multi-panel shapes, both operand layouts, pinned and pageable
 buffers, K = 0, and back-to-back calls that reuse the handle's device copies."""
 import itertools
@@ -46,9 +46,11 @@ def run_host(h, p, pinned=True, out=None):
     return c
 
 
-# (M, N, K): one panel; two panels with a ragged tail; four panels; an output row of
-# 1001 fp32 values (not a multiple of 16 bytes, so the device copy is padded)
-HOST_SHAPES = [(1, 1, 1), (300, 257, 65), (4500, 130, 96), (8200, 72, 40), (2049, 1001, 33)]
+# (M, N, K): one panel each; several row panels of A with a ragged tail; an output row of
+# 1001 fp32 values (not a multiple of 16 bytes, so the device copy is padded); several
+# panels of both operands
+HOST_SHAPES = [(1, 1, 1), (300, 257, 65), (4500, 130, 96), (8200, 72, 40), (2049, 1001, 33),
+               (1500, 3000, 24)]
 
 
 @pytest.mark.parametrize("dtype,precision", [("bf16", "default"), ("f32", "exact")])
@@ -61,6 +63,23 @@ def test_host_path_integer_bit_exact(h, dtype, precision, a_layout, b_layout):
         assert not c.is_cuda
         ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
         assert torch.equal(c.to(torch.int64), ref), (M, N, K)
+
+
+@pytest.mark.parametrize("panel", [256, 1024, 1 << 20])
+def test_host_path_panel_widths(panel):
+    """Explicit panel widths: many 256-wide panels (more than the 32-panel cap, which
+    widens them), the default-sized ones, and one panel per operand."""
+    import dense_tiled_gemm_05_gb300 as g
+    hh = g.Gemm(0)
+    hh.set_option("host_panel", panel)
+    for n, (M, N, K) in enumerate([(4500, 1300, 96), (257, 64, 64), (9000, 700, 48),
+                                   (300, 9001, 40)]):
+        p = W.integer_problem(M, N, K, "bf16", seed=700 + n, b_layout="col")
+        c = run_host(hh, p)
+        assert torch.equal(c.to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    with pytest.raises(g.GemmError):
+        hh.set_option("host_panel", 100)
+    hh.close()
 
 
 def test_host_path_random_vs_oracle(h):
