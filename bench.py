@@ -1,7 +1,7 @@
 """Benchmark of the GB300 blocked GEMM library; prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload bf16_8192|bf16_4096|tf32_4096|exact_4096|bf16_skinny]
+                    [--workload bf16_8192|bf16_4096|tf32_4096|exact_4096|f16acc_4096|bf16_skinny]
 
 A step is one C = A @ B over one batch of seeded synthetic inputs already resident
 in HBM. Default workload: bf16 M = N = K = 8192, A row-major, B column-major,
@@ -63,6 +63,10 @@ def workload(name):
         return (W.fp32_square(4096, "exact"), "fp32 GEMM M=N=K=4096 row-major, U[-1,1], "
                 "exact-fp32 mode (split-tf32, three tensor-core products), fp32 out",
                 "tensor_x3")
+    if name == "f16acc_4096":
+        return (W.f16acc_square(4096), "fp16 GEMM M=N=K=4096, A row-major, B column-major, "
+                "N(0,1)*0.1, fp16 accumulator rounded every 16 K (section 13.3), fp16 out",
+                "tensor")
     if name == "bf16_skinny":
         return (W.bf16_skinny(), "bf16 GEMM M=16384 N=128 K=8192, A row-major, B column-major, "
                 "N(0,1)/sqrt(K), fp32 accumulate, bf16 out (memory-bound)", "hbm")
@@ -158,47 +162,65 @@ class ClockSampler:
                 "power_w_max": max(x["power"] for x in s)}
 
 
-def cpu_baseline(p, target_s=10.0):
-    """The oracle as it stands on a bounded sample of output rows (all columns)."""
+F16ACC_CHUNK = 16  # the library's default fp16-accumulator chunk
+
+
+def oracle_block(p):
+    """f(rows, c): the oracle's values of C[rows, :c] for the workload's arithmetic (the
+    fp64 product, or the fp16 accumulator's chunked definition)."""
     import oracle
     a, al, lda = W.storage_numpy(p.A)
     b, bl, ldb = W.storage_numpy(p.B)
-    kw = dict(lda=lda, ldb=ldb, a_dtype=p.in_dtype, b_dtype=W.dtype_name(p.B.dtype),
-              a_layout=al, b_layout=bl)
+    bdt = W.dtype_name(p.B.dtype)
+    if p.precision == "f16acc":
+        assert al == "row"
+
+        def f(rows, c):
+            sub = np.stack([a[i * lda:i * lda + p.K] for i in rows])
+            return oracle.gemm_f16acc(sub, b, len(rows), c, p.K, lda=p.K, ldb=ldb,
+                                      a_dtype="f16", b_dtype=bdt, BK=F16ACC_CHUNK,
+                                      b_layout=bl)
+        return f
+    kw = dict(lda=lda, ldb=ldb, a_dtype=p.in_dtype, b_dtype=bdt, a_layout=al, b_layout=bl)
+    return lambda rows, c: oracle.gemm_f64(a, b, p.M, c, p.K, rows=rows, **kw)
+
+
+def cpu_baseline(p, target_s=10.0):
+    """The oracle as it stands on a bounded sample of output rows (all columns)."""
+    import oracle
+    f = oracle_block(p)
     # Calibrate: the per-call cost is a fixed part (decoding B) plus a per-row part.
     times = {}
     for r in (4, 12):
         t0 = time.perf_counter()
-        oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=np.arange(r), **kw)
+        f(np.arange(r), p.N)
         times[r] = time.perf_counter() - t0
     per_row = max((times[12] - times[4]) / 8, 1e-6)
     fixed = max(times[4] - 4 * per_row, 0.0)
     rows = int(max(8, min(p.M, (target_s - fixed) / per_row)))
     sel = np.linspace(0, p.M - 1, rows).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.gemm_f64(a, b, p.M, p.N, p.K, rows=sel, **kw)
+    f(sel, p.N)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * p.N * p.K
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    cores = 1 if p.precision == "f16acc" else oracle.num_threads()
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
-            "sample": "%d of %d output rows (all %d columns, K=%d) in fp64, %.1f s, OpenMP"
-                      % (rows, p.M, p.N, p.K, dt)}
+            "sample": "%d of %d output rows (all %d columns, K=%d) in fp64, %.1f s, %s"
+                      % (rows, p.M, p.N, p.K, dt,
+                         "fp16 accumulator, 1 thread" if p.precision == "f16acc" else "OpenMP")}
 
 
 def run_reference(args, p, desc):
     """--impl reference: the CPU oracle timed per step on a bounded block of the output."""
     import oracle
-    a, al, lda = W.storage_numpy(p.A)
-    b, bl, ldb = W.storage_numpy(p.B)
-    kw = dict(lda=lda, ldb=ldb, a_dtype=p.in_dtype, b_dtype=W.dtype_name(p.B.dtype),
-              a_layout=al, b_layout=bl)
+    f = oracle_block(p)
     # One step computes an r x c block of C over the full K: rows spread over M, and the
     # first c columns of B (same storage and leading dimension, so only they are decoded).
     budget = 120.0 / max(1, args.steps + args.warmup)
 
     def block(r, c, i0):
-        rows = (np.arange(r) * 7919 + i0) % p.M
-        return oracle.gemm_f64(a, b, p.M, c, p.K, rows=rows, **kw)
+        return f((np.arange(r) * 7919 + i0) % p.M, c)
 
     r = c = 32
     t0 = time.perf_counter()
@@ -215,8 +237,10 @@ def run_reference(args, p, desc):
     dt = time.perf_counter() - t0
     flops = 2.0 * r * c * p.K * args.steps
     value = flops / dt / 1e12
-    cores = oracle.num_threads()
-    sample = "per step a %d x %d block of C over K=%d, fp64 oracle, OpenMP" % (r, c, p.K)
+    f16acc = p.precision == "f16acc"
+    cores = 1 if f16acc else oracle.num_threads()
+    sample = "per step a %d x %d block of C over K=%d, %s" % (
+        r, c, p.K, "fp16-accumulator oracle, 1 thread" if f16acc else "fp64 oracle, OpenMP")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",

@@ -25,15 +25,16 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libgemm_gb300.so")
 
 # enums of include/gemm.h
 F32, F16, BF16 = 0, 1, 2
-PREC = {"default": 0, "tf32": 1, "exact": 2}
+PREC = {"default": 0, "tf32": 1, "exact": 2, "f16acc": 3}
 ROW, COL = 0, 1
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
           3: "GEMM_ERR_ALIGNMENT", 4: "GEMM_ERR_NO_MEMORY", 5: "GEMM_ERR_CUDA",
           6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_DEVICE"}
 OPTIONS = {"wait_timeout_us": 0, "force_path": 1, "group_m": 2, "max_ctas": 3,
            "fault_stall_producer": 4, "force_staging": 5, "cta_pair": 6,
-           "block_n": 7, "exact_chunk": 8, "stream_k": 9, "host_panel": 10}
-PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma", 4: "tcgen05_3xtf32"}
+           "block_n": 7, "exact_chunk": 8, "stream_k": 9, "host_panel": 10, "acc_chunk": 11}
+PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma", 4: "tcgen05_3xtf32",
+         5: "tcgen05_f16acc"}
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 _DT_NAMES = {"f32": F32, "f16": F16, "bf16": BF16}
 _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}

@@ -7,7 +7,10 @@
 // by rows < M, k < K and cols < N with zeros outside (section 13.2's three masks), and a
 // store masked by rows < M and cols < N. It serves the exact-fp32 mode ("Triton matmul",
 // the "Precision" section: tf32 is not exact) and, with 4 x 4 x 4 tiles, the pages' own
-// 8 x 8 x 8 example (grid 2 x 2, two K-iterations per tile).
+// 8 x 8 x 8 example (grid 2 x 2, two K-iterations per tile). With an fp16 accumulator
+// (section 13.3, Worked Example 13.3.1) each K-chunk's dot product is summed in fp32, then
+// rounded to fp16 and added to the fp16 running total, itself rounded to fp16 after every
+// chunk; the chunk is a multiple of BK, so with BK = 8 it can be the pages' own BLOCK_K.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,7 +50,15 @@ __device__ __forceinline__ int owned(int t, int i) {
   return t * T + i;
 }
 
-template <int BM, int BN, int BK, int TM, int TN, typename InT>
+// fp16(acc + fp16(partial)) for acc holding an fp16 value: the fp32 sum of two fp16 values
+// rounded to fp16 equals their correctly rounded fp16 sum (fp32 carries 24 >= 2 * 11 + 2
+// significand bits, so the double rounding is innocuous).
+__device__ __forceinline__ float f16_accumulate(float acc, float partial) {
+  const float h = __half2float(__float2half_rn(partial));
+  return __half2float(__float2half_rn(acc + h));
+}
+
+template <int BM, int BN, int BK, int TM, int TN, typename InT, bool F16ACC>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
     fma_gemm_kernel(const FmaParams p) {
   constexpr int TX = BN / TN, TY = BM / TM, NT = TX * TY;
@@ -58,11 +69,18 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
 
-  float acc[TM][TN];
+  float acc[TM][TN];   // fp32 accumulator, or the chunk's partial dot (fp16 accumulator)
+  float hacc[F16ACC ? TM : 1][F16ACC ? TN : 1];  // fp16 running total (fp16 accumulator)
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;  // initialised once, before the K-loop
+  if (F16ACC) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) hacc[F16ACC ? i : 0][F16ACC ? j : 0] = 0.0f;
+  }
 
   for (int64_t k0 = 0; k0 < p.K; k0 += BK) {
     // A tile: rows m0.., k-columns k0..; walk the storage's contiguous axis fastest.
@@ -96,6 +114,22 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
         for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     __syncthreads();
+    if (F16ACC && ((k0 + BK) % p.acc_chunk == 0 || k0 + BK >= p.K)) {  // chunk done
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          float &h = hacc[F16ACC ? i : 0][F16ACC ? j : 0];
+          h = f16_accumulate(h, acc[i][j]);
+          acc[i][j] = 0.0f;
+        }
+    }
+  }
+  if (F16ACC) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) acc[i][j] = hacc[F16ACC ? i : 0][F16ACC ? j : 0];
   }
 
 #pragma unroll
@@ -115,12 +149,16 @@ cudaError_t fma_launch_tile(const FmaParams &p, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>((p.N + BN - 1) / BN),
                   static_cast<unsigned>((p.M + BM - 1) / BM));
   const dim3 block((BM / TM) * (BN / TN));
-  if (p.in_dtype == GEMM_F32)
-    fma_gemm_kernel<BM, BN, BK, TM, TN, float><<<grid, block, 0, s>>>(p);
-  else if (p.in_dtype == GEMM_F16)
-    fma_gemm_kernel<BM, BN, BK, TM, TN, __half><<<grid, block, 0, s>>>(p);
-  else
-    fma_gemm_kernel<BM, BN, BK, TM, TN, __nv_bfloat16><<<grid, block, 0, s>>>(p);
+  if (p.acc_chunk > 0) {
+    if (p.in_dtype != GEMM_F16 || p.acc_chunk % BK) return cudaErrorInvalidValue;
+    fma_gemm_kernel<BM, BN, BK, TM, TN, __half, true><<<grid, block, 0, s>>>(p);
+  } else if (p.in_dtype == GEMM_F32) {
+    fma_gemm_kernel<BM, BN, BK, TM, TN, float, false><<<grid, block, 0, s>>>(p);
+  } else if (p.in_dtype == GEMM_F16) {
+    fma_gemm_kernel<BM, BN, BK, TM, TN, __half, false><<<grid, block, 0, s>>>(p);
+  } else {
+    fma_gemm_kernel<BM, BN, BK, TM, TN, __nv_bfloat16, false><<<grid, block, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

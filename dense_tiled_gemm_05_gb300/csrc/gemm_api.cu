@@ -39,6 +39,7 @@ struct gemm_handle_s {
   int cta_pair = 0;  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
   int block_n = 0;   // 0 auto, else 128 or 256
   int exact_chunk = 0;  // 0 default
+  int acc_chunk = 0;    // fp16-accumulator chunk in K elements, 0 default (16)
   int stream_k = 0;     // 0 auto (on), 1 off
   int host_panel = 0;  // gemm_run_host panel width (rows of A, columns of B), 0 auto
   // split-K workspace of the CTA-pair kernel: partial tiles and flags
@@ -134,14 +135,19 @@ struct Problem {
 
 struct Options {
   int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
-  int stream_k = 0;
+  int stream_k = 0, exact_chunk = 0, acc_chunk = 0;
 };
+
+// fp16-accumulator chunk (K elements per fp16 rounding of the running total) when the
+// caller sets none: the K of one tcgen05.mma.kind::f16.
+constexpr int kDefaultAccChunk = 16;
 
 // An operand as the tensor-core kernel sees it: `outer` lines of `inner` contiguous
 // elements with leading dimension ld (in elements). It is either read in place or staged
 // into the workspace first: copied when TMA cannot address it (misaligned base or
-// leading dimension), transposed into K-major form when it is an MN-major tf32 operand
-// (the tf32 tensor-core instruction reads K-major operands only), or split into tf32
+// leading dimension), transposed into K-major form when it is an MN-major operand of a
+// kernel that reads K-major operands only (tf32, which the tensor cores take K-major only
+// on GB300, and the fp16-accumulator kernel), or split into tf32
 // hi/lo parts (exact-fp32 mode; always K-major, 3K columns).
 struct OperandPlan {
   const void *ptr;          // caller's operand
@@ -160,13 +166,15 @@ struct Plan {
   TcVariant variant;
   OperandPlan a, b;
   int fma_tile;
+  int chunk_steps;    // chunked tensor-core kernel: MMA instructions per TMEM partial
+  int64_t acc_chunk;  // fp16 accumulator: K elements per rounding (0: fp32 accumulator)
 };
 
 gemm_status_t check_args(const Problem &P) {
   if (P.M < 0 || P.N < 0 || P.K < 0) return GEMM_ERR_INVALID_ARG;
   if (!valid_dtype(P.in_dtype) || !valid_dtype(P.out_dtype)) return GEMM_ERR_INVALID_ARG;
   if (!valid_layout(P.a_layout) || !valid_layout(P.b_layout)) return GEMM_ERR_INVALID_ARG;
-  if (P.precision < GEMM_PREC_DEFAULT || P.precision > GEMM_PREC_EXACT_FP32)
+  if (P.precision < GEMM_PREC_DEFAULT || P.precision > GEMM_PREC_F16_ACC)
     return GEMM_ERR_INVALID_ARG;
   const bool a_used = P.M > 0 && P.K > 0 && P.N > 0;
   const bool b_used = P.K > 0 && P.N > 0 && P.M > 0;
@@ -182,7 +190,11 @@ gemm_status_t check_args(const Problem &P) {
     if (!P.B) return GEMM_ERR_INVALID_ARG;
     if (P.ldb < (P.b_layout == GEMM_ROW_MAJOR ? P.N : P.K)) return GEMM_ERR_INVALID_ARG;
   }
-  if (P.in_dtype != GEMM_F32 && P.precision != GEMM_PREC_DEFAULT) return GEMM_ERR_UNSUPPORTED;
+  if (P.precision == GEMM_PREC_F16_ACC) {
+    if (P.in_dtype != GEMM_F16) return GEMM_ERR_UNSUPPORTED;  // the pages' fp16 inputs only
+  } else if (P.in_dtype != GEMM_F32 && P.precision != GEMM_PREC_DEFAULT) {
+    return GEMM_ERR_UNSUPPORTED;
+  }
   if (P.M > INT32_MAX || P.N > INT32_MAX || P.K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   const int es = esize_of(P.in_dtype), os = esize_of(P.out_dtype);
   if ((a_used && reinterpret_cast<uintptr_t>(P.A) % es) ||
@@ -215,7 +227,7 @@ bool tma_legal(const void *p, int64_t ld, int64_t outer, int es) {
 
 OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout,
                          bool k_is_rows_dim, int es, bool force_stage, bool split3,
-                         size_t *ws_cursor) {
+                         bool k_major_only, size_t *ws_cursor) {
   OperandPlan o{};
   o.ptr = p;
   o.ld = ld;
@@ -231,7 +243,7 @@ OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, 
   o.k_outer = o.outer;
   o.k_inner = o.inner;
   o.split3 = split3;
-  o.transpose = !split3 && o.mn_major && es == 4;
+  o.transpose = !split3 && o.mn_major && (es == 4 || k_major_only);
   o.staged = split3 || o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
   if (o.staged) {
     if (split3) {
@@ -304,16 +316,24 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   }
   // Exact fp32 runs on the tensor cores as three tf32 products of split operands, except
   // for tiny problems (the pages' 8 x 8 example and smaller), which take the fp32 FMA
-  // kernel with 4 x 4 x 4 tiles; GEMM_OPT_FORCE_PATH chooses either explicitly.
+  // kernel with 4 x 4 x 4 tiles; GEMM_OPT_FORCE_PATH chooses either explicitly. The fp16
+  // accumulator runs on the tensor cores when its chunk is a whole number of 16-long MMAs,
+  // else (e.g. the pages' BLOCK_K = 8) on the FMA kernel, whose K-tile is 8.
   const bool exact = P.in_dtype == GEMM_F32 && P.precision != GEMM_PREC_TF32;
-  bool use_fma = exact && P.M * P.N <= 256;
+  const bool f16acc = P.precision == GEMM_PREC_F16_ACC;
+  pl.acc_chunk = f16acc ? (opt.acc_chunk > 0 ? opt.acc_chunk : kDefaultAccChunk) : 0;
+  bool use_fma = (exact && P.M * P.N <= 256) || (f16acc && pl.acc_chunk % 16 != 0);
   if (opt.force_path == 2) use_fma = true;
-  if (opt.force_path == 1) use_fma = false;
+  if (opt.force_path == 1) {
+    if (f16acc && pl.acc_chunk % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    use_fma = false;
+  }
   const bool split = exact && !use_fma;
   if (use_fma) {
-    pl.fma_tile = (P.M * P.N <= 256) ? 4 : 128;
+    pl.fma_tile = (P.M * P.N <= 256 && !f16acc) ? 4 : 128;
     int bm, bn, bk;
     fma_tile_shape(pl.fma_tile, &bm, &bn, &bk);
+    if (pl.acc_chunk % bk) return GEMM_ERR_UNSUPPORTED;
     I.path = GEMM_PATH_FMA;
     I.tile_m = bm, I.tile_n = bn, I.tile_k = bk;
     I.grid_m = (P.M + bm - 1) / bm;
@@ -328,9 +348,9 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   const int os = esize_of(P.out_dtype);
   size_t cursor = 0;
   pl.a = plan_operand(P.A, P.M, P.K, P.lda, P.a_layout, false, es, opt.force_staging != 0, split,
-                      &cursor);
+                      f16acc, &cursor);
   pl.b = plan_operand(P.B, P.K, P.N, P.ldb, P.b_layout, true, es, opt.force_staging != 0, split,
-                      &cursor);
+                      f16acc, &cursor);
   pl.variant.esize = es;
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
@@ -341,12 +361,14 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
       opt.block_n ? opt.block_n
                   : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
                                  split ? 1 : opt.stream_k, sm_count);
-  if (split) {  // the exact-fp32 kernel has one shape: CTA pairs, 256 x 256 tiles
-    pl.variant.exact = true;
+  if (split || f16acc) {  // the chunked kernel has one shape: CTA pairs, 256 x 256 tiles
+    pl.variant.exact = split;
+    pl.variant.f16acc = f16acc;
     pl.variant.pair = true;
     pl.variant.block_n = 256;
   }
-  I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : GEMM_PATH_TCGEN05;
+  const bool chunked = pl.variant.exact || pl.variant.f16acc;
+  I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : f16acc ? GEMM_PATH_TCGEN05_F16ACC : GEMM_PATH_TCGEN05;
   I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
   I.tile_n = pl.variant.block_n;
   I.tile_k = 128 / es;
@@ -355,6 +377,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   const int64_t k_total = split ? 3 * P.K : P.K;  // split operands concatenate 3 products
   I.k_iters = (k_total + I.tile_k - 1) / I.tile_k;
   if (I.grid_m * I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  // chunked kernel: four MMAs per 128-byte K-block
+  if (split)
+    pl.chunk_steps = 4 * (opt.exact_chunk > 0 ? opt.exact_chunk : exact_chunk_kblocks(I.k_iters));
+  else if (f16acc)
+    pl.chunk_steps = static_cast<int>(pl.acc_chunk / 16);
   I.stages = tc_stages(pl.variant);
   I.stage_a = pl.a.staged, I.stage_b = pl.b.staged;
   I.a_mn_major = pl.a.mn_major, I.b_mn_major = pl.b.mn_major;
@@ -369,7 +396,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
     // With a split-K share every cluster takes part, even when there are fewer tiles.
     int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
     if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
-    const bool split = !pl.variant.exact && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
+    const bool split = !chunked && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
                        sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(I.k_iters),
                                    static_cast<int32_t>(clusters), true) < tiles;
     I.ctas = 2 * (split || tiles > clusters ? clusters : tiles);
@@ -380,7 +407,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   }
   I.workspace_bytes = static_cast<int64_t>(cursor);
   I.cta_pair = pl.variant.pair ? 1 : 0;
-  if (pl.variant.pair && !pl.variant.exact) {
+  if (pl.variant.pair && !chunked) {
     const int32_t slots = static_cast<int32_t>(I.ctas / 2);
     const int32_t t = static_cast<int32_t>(tiles);
     if (use_split_k(opt.stream_k, t, I.k_iters, slots))
@@ -461,6 +488,8 @@ Options options_of(gemm_handle_t h) {
     o.cta_pair = h->cta_pair;
     o.block_n = h->block_n;
     o.stream_k = h->stream_k;
+    o.exact_chunk = h->exact_chunk;
+    o.acc_chunk = h->acc_chunk;
   }
   return o;
 }
@@ -507,8 +536,7 @@ gemm_status_t ensure_sk_workspace(gemm_handle_t h, size_t bytes, size_t flag_byt
 
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
                         const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,
-                        int group_m, int debug_flags, int exact_chunk, SplitK sk,
-                        cudaStream_t s) {
+                        int group_m, int debug_flags, SplitK sk, cudaStream_t s) {
   const gemm_plan_info_t &I = pl.info;
   const int es = esize_of(P.in_dtype);
   const uint32_t row_elems = 128 / es;  // elements in one 128-byte swizzle row
@@ -546,17 +574,19 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   tp.status = status;
   tp.timeout_ns = timeout_ns;
   tp.debug_flags = debug_flags;
-  tp.chunk_kblocks = exact_chunk > 0 ? exact_chunk : exact_chunk_kblocks(I.k_iters);
+  tp.chunk_steps = pl.chunk_steps;
   int64_t grid = I.ctas;
   if (pl.variant.pair) {
-    const int64_t fit = pl.variant.exact ? tc_exact_max_active_clusters() : tc2_max_active_clusters();
+    const int64_t fit = pl.variant.exact || pl.variant.f16acc
+                            ? tc_chunk_max_active_clusters(pl.variant.f16acc)
+                            : tc2_max_active_clusters();
     if (fit <= 0) return GEMM_ERR_CUDA;
     if (grid / 2 > fit) grid = 2 * fit;
   }
   // Split-K share of the last rounds (CTA-pair kernel): whole tiles otherwise.
   const int32_t tiles = tp.tiles_m * tp.tiles_n;
   tp.sk_dp_tiles = tiles;
-  if (pl.variant.pair && !pl.variant.exact && sk.h) {
+  if (pl.variant.pair && !pl.variant.exact && !pl.variant.f16acc && sk.h) {
     const int32_t slots = static_cast<int32_t>(grid / 2);
     tp.sk_dp_tiles = sk_dp_tiles(tiles, tp.k_blocks, slots,
                                  use_split_k(sk.mode, tiles, tp.k_blocks, slots));
@@ -593,7 +623,7 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
       return GEMM_OK;
     case GEMM_PATH_FMA: {
       FmaParams fp{P.M, P.N, P.K, P.A, P.lda, P.B, P.ldb, P.C, P.ldc, P.in_dtype, P.out_dtype,
-                   P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR};
+                   P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR, pl.acc_chunk};
       e = fma_launch(fp, pl.fma_tile, s);
       if (e != cudaSuccess) return cuda_fail(e, "fma launch");
       h->launches += 1;
@@ -624,7 +654,7 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   sk.h = h;
   sk.mode = h->stream_k;
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
-                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, h->exact_chunk, sk, s);
+                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, sk, s);
   if (st != GEMM_OK) return st;
   h->launches += 1;
   return GEMM_OK;
@@ -743,6 +773,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
     case GEMM_OPT_CTA_PAIR:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_ACC_CHUNK:
+      if (v < 0 || v > (int64_t{1} << 20) || v % 8) return GEMM_ERR_INVALID_ARG;
+      h->acc_chunk = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_HOST_PANEL:
       if (v < 0 || v > (int64_t{1} << 30) || v % 256) return GEMM_ERR_INVALID_ARG;
@@ -1049,7 +1083,7 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
       return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "zero fill launch");
     case GEMM_PATH_FMA: {
       FmaParams fp{P.M, P.N, P.K, P.A, P.lda, P.B, P.ldb, P.C, P.ldc, P.in_dtype, P.out_dtype,
-                   P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR};
+                   P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR, pl.acc_chunk};
       e = fma_launch(fp, pl.fma_tile, s);
       return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "fma launch");
     }
@@ -1086,7 +1120,7 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
   }
   const Options defaults;
   return launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, status, gemm_handle_s().timeout_us * 1000ull,
-                   defaults.group_m, 0, 0, SplitK(), s);
+                   defaults.group_m, 0, SplitK(), s);
 }
 
 }  // namespace

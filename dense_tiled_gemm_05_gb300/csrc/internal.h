@@ -29,7 +29,7 @@ struct TcParams {
   int *status;         // device status word
   uint64_t timeout_ns; // bounded-wait limit
   int32_t debug_flags;
-  int32_t chunk_kblocks;  // exact-fp32 kernel: K-blocks per TMEM partial sum
+  int32_t chunk_steps;    // chunked kernel: MMA instructions per TMEM partial sum
   // split-K share of the last rounds (CTA-pair kernel; see sk_schedule.h)
   int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
   float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32
@@ -44,7 +44,8 @@ struct TcVariant {
   bool a_mn, b_mn;
   int block_n;
   bool pair;   // CTA pair (cta_group::2): 256-row tiles over two SMs
-  bool exact;  // exact-fp32 kernel on split operands (CTA pairs, chunked fp32 sums)
+  bool exact;   // exact-fp32 kernel on split operands (CTA pairs, chunked fp32 sums)
+  bool f16acc;  // fp16-accumulator kernel (CTA pairs, chunk dots rounded into fp16 sums)
 };
 
 int tc_stages(const TcVariant &v);
@@ -58,10 +59,11 @@ cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtenso
                        cudaStream_t s);
 // Clusters of two CTAs of the pair kernel that fit on the current device at once.
 int tc2_max_active_clusters();
-// Exact-fp32 kernel (CTA pairs, 256 x 256 tiles, split tf32 operands, chunked sums).
-cudaError_t tc_exact_launch(const CUtensorMap &tmA, const CUtensorMap &tmB,
+// Chunked kernel (CTA pairs, 256 x 256 tiles, K-major operands, register accumulators):
+// exact fp32 on split tf32 operands, or (f16acc) fp16 inputs with an fp16 accumulator.
+cudaError_t tc_chunk_launch(bool f16acc, const CUtensorMap &tmA, const CUtensorMap &tmB,
                             const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
-int tc_exact_max_active_clusters();
+int tc_chunk_max_active_clusters(bool f16acc);
 // K-blocks of 32 split products the exact kernel accumulates in TMEM before adding the
 // partial into its fp32 register sums. The tensor cores' accumulation keeps fewer bits
 // than an IEEE fp32 add, and its error relative to sum |a b| is largest for short K, so
@@ -83,6 +85,7 @@ struct FmaParams {
   int64_t ldc;
   int32_t in_dtype, out_dtype;
   int32_t a_col, b_col;  // 1 = column-major operand
+  int64_t acc_chunk;     // > 0: fp16 accumulator rounded every acc_chunk K (a multiple of BK)
 };
 // tile: 4 selects the 4x4x4 tiles of the pages' 8x8x8 example, anything else 128x128x8.
 cudaError_t fma_launch(const FmaParams &p, int tile, cudaStream_t s);

@@ -1,22 +1,32 @@
-// tc_exact_kernel.cu -- exact-fp32 GEMM on the tensor cores (CTA pairs, chunked sums).
+// tc_chunk_kernel.cu -- tensor-core GEMMs whose accumulator lives in registers and takes
+// the tensor cores' fp32 partial products one short K-chunk at a time (CTA pairs).
 //
-// Exact fp32 ("Triton matmul", "Precision": fp32 inputs need an explicit choice between
-// tf32 and full fp32 accuracy) runs on the tf32 tensor cores: split_kernel.cu writes
-// A' = [hi(A) | hi(A) | lo(A)] and B' = [hi(B) ; lo(B) ; hi(B)] so that A' B' holds the three
-// significant partial products of the split operands. The tensor cores' fp32 accumulation
-// over a long K drifts (measured on GB300: 4e-6 of sum |a b| at K = 4096, growing with K),
-// so this kernel never lets one TMEM accumulator run over more than a short chunk of K':
-// the MMA issuer alternates between two TMEM accumulators every `chunk` K-blocks, and the
-// epilogue warps add each finished chunk into fp32 registers with ordinary IEEE adds. The
-// tile's structure is otherwise the blocked matmul of "Chapter 13: The Blocked Matmul
-// Kernel", section 13.1: the register sum starts at zero once per tile, every K-chunk's
-// partial product is added to it, and the result is rounded once at the store (13.3).
+// Two modes share the kernel; both keep the tile structure of the blocked matmul of
+// "Chapter 13: The Blocked Matmul Kernel", section 13.1 (the accumulator starts at zero once
+// per tile, every K-chunk's partial product is added to it, the result is stored once),
+// and both let the MMA issuer alternate between two TMEM accumulators, starting a fresh one
+// every `chunk_steps` MMA instructions, while the epilogue warps add each finished chunk
+// into their registers.
+//
+// * Exact fp32 ("Triton matmul", "Precision": fp32 inputs need an explicit choice between
+//   tf32 and full fp32 accuracy) on the tf32 tensor cores: split_kernel.cu writes
+//   A' = [hi(A) | hi(A) | lo(A)] and B' = [hi(B) ; lo(B) ; hi(B)] so that A' B' holds the
+//   three significant partial products of the split operands. The tensor cores' fp32
+//   accumulation over a long K drifts (measured on GB300: 4e-6 of sum |a b| at K = 4096,
+//   growing with K), so no TMEM accumulator runs over more than a short chunk, and the
+//   chunks are summed in fp32 registers with ordinary IEEE adds; rounded once at the store.
+//
+// * fp16 accumulator (section 13.3, Worked Example 13.3.1): fp16 inputs, and an
+//   accumulator held in fp16 that rounds after every K-chunk: each chunk's dot product
+//   (fp32, from the tensor cores) is rounded to fp16 and added to the fp16 running total
+//   with an fp16 add (round to nearest even). One chunk is a multiple of the 16-long K of
+//   one tcgen05.mma.kind::f16.
 //
 // Roles (320 threads per CTA, clusters of two CTAs, 256 x 256 tile per cluster):
-//   warp 0      TMA producer (both CTAs): 128 rows of A', 128 columns of B' per K-block;
-//   warp 1      MMA issuer (leader CTA): tcgen05.mma.cta_group::2.kind::tf32, M=256, N=256;
+//   warp 0      TMA producer (both CTAs): 128 rows of A, 128 columns of B per 128-byte K-block;
+//   warp 1      MMA issuer (leader CTA): tcgen05.mma.cta_group::2, M=256, N=256;
 //   warps 2-9   epilogue (both CTAs): warp w reads TMEM lanes 32*(w%4).. and one 128-column
-//               half of the tile, keeps 128 fp32 sums per thread, stores once per tile.
+//               half of the tile, keeps 128 running sums per thread, stores once per tile.
 #include "tc_common.cuh"
 
 namespace gemm_gb300 {
@@ -27,15 +37,17 @@ using namespace tc;
 constexpr int kXThreads = 320;
 constexpr int kXEpiWarps = 8;
 
+template <bool F16ACC>
 struct CfgX {
+  static constexpr int ES = F16ACC ? 2 : 4;     // bytes per operand element
   static constexpr int BM = kTcBlockM;          // rows per CTA (256 per pair)
   static constexpr int BN = 256;                // columns per pair tile
-  static constexpr int BN_HALF = BN / 2;        // B' columns loaded by each CTA
-  static constexpr int BK = kRowBytes / 4;      // 32 fp32 per K-block
-  static constexpr int UMMA_K = 8;              // K per tcgen05.mma.kind::tf32
+  static constexpr int BN_HALF = BN / 2;        // B columns loaded by each CTA
+  static constexpr int BK = kRowBytes / ES;     // elements per 128-byte K-block
+  static constexpr int UMMA_K = F16ACC ? 16 : 8;  // K per tcgen05.mma (kind::f16 / kind::tf32)
   static constexpr int K_STEPS = BK / UMMA_K;
-  static constexpr int A_BYTES = BM * BK * 4;
-  static constexpr int B_BYTES = BN_HALF * BK * 4;
+  static constexpr int A_BYTES = BM * kRowBytes;
+  static constexpr int B_BYTES = BN_HALF * kRowBytes;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = 6;
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
@@ -45,19 +57,21 @@ struct CfgX {
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int COLS = 128;  // columns per epilogue thread
+  static_assert(K_STEPS == 4, "four MMAs per K-block");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
+constexpr int kXCols = 128;
 
 // Store one warp's 32 x 128 block from registers through the 128B-swizzled staging box.
 template <int OUT>
-__device__ __forceinline__ void store_regs_tma(const float (&v)[CfgX::COLS], const CUtensorMap *tmC,
+__device__ __forceinline__ void store_regs_tma(const float (&v)[kXCols], const CUtensorMap *tmC,
                                                uint8_t *sb, int lane, int row0, int col0, int M,
                                                int N) {
   constexpr int OUT_COLS = OUT == GEMM_F32 ? 32 : 64;
   if (row0 >= M) return;  // warp-uniform
 #pragma unroll
-  for (int b = 0; b < CfgX::COLS / OUT_COLS; ++b) {
+  for (int b = 0; b < kXCols / OUT_COLS; ++b) {
     if (col0 + b * OUT_COLS >= N) break;  // warp-uniform
     if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
@@ -92,13 +106,13 @@ __device__ __forceinline__ void store_regs_tma(const float (&v)[CfgX::COLS], con
 
 // Store one thread's row segment from registers with plain masked stores.
 template <int OUT>
-__device__ __forceinline__ void store_regs_direct(const float (&v)[CfgX::COLS], const TcParams &p,
+__device__ __forceinline__ void store_regs_direct(const float (&v)[kXCols], const TcParams &p,
                                                   int row, int col0) {
   if (row >= p.M || col0 >= p.N) return;
-  const int n = min(CfgX::COLS, p.N - col0);
+  const int n = min(kXCols, p.N - col0);
   const int64_t base = static_cast<int64_t>(row) * p.ldc + col0;
 #pragma unroll
-  for (int j = 0; j < CfgX::COLS; ++j) {
+  for (int j = 0; j < kXCols; ++j) {
     if (j < n) {
       if (OUT == GEMM_F32)
         reinterpret_cast<float *>(p.C)[base + j] = v[j];
@@ -110,10 +124,21 @@ __device__ __forceinline__ void store_regs_direct(const float (&v)[CfgX::COLS], 
   }
 }
 
+template <int OUT>
+__device__ __forceinline__ void store_regs(const float (&v)[kXCols], const CUtensorMap *tmC,
+                                           uint8_t *sb, const TcParams &p, int lane, int row0,
+                                           int col0) {
+  if (p.tma_store)
+    store_regs_tma<OUT>(v, tmC, sb, lane, row0, col0, p.M, p.N);
+  else
+    store_regs_direct<OUT>(v, p, row0 + lane, col0);
+}
+
+template <bool F16ACC>
 __global__ void __launch_bounds__(kXThreads, 1)
-    tc_exact_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    tc_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using G = CfgX;
+  using G = CfgX<F16ACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -129,7 +154,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   const int lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
-  const int chunk = p.chunk_kblocks;
+  const int chunk = p.chunk_steps;  // MMA instructions per TMEM partial
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::STAGES; ++s) {
@@ -193,17 +218,31 @@ __global__ void __launch_bounds__(kXThreads, 1)
     if (leader && lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      // Four MMAs per K-block. When chunks are whole K-blocks (always in exact mode) the
+      // chunk decisions are taken once per K-block and the four MMAs issue back to back:
+      // this single thread's issue rate bounds the kernel, and per-MMA branching was
+      // measured to cost up to half of the throughput.
+      const bool by_block = chunk % G::K_STEPS == 0;
+      const int chunk_kb = by_block ? chunk / G::K_STEPS : 1;
+      auto take_acc = [&](uint32_t &d_tmem) {  // a fresh accumulator for the next chunk
+        if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, wd)) return false;
+        tc_fence_after();
+        d_tmem = tmem_base + acc * G::BN;
+        return true;
+      };
+      auto hand_over = [&]() {  // chunk done: the epilogue may read it
+        mma_commit_pair_multicast(&tmem_full[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      };
       for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
         uint32_t d_tmem = 0;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          const int in_chunk = kb % chunk;
-          if (in_chunk == 0) {  // a fresh accumulator for this chunk of K'
-            if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, wd)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            d_tmem = tmem_base + acc * G::BN;
+        int left = 0;  // per-MMA chunks: MMAs left in the current chunk (0: start one)
+        for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
+          const int in_chunk = by_block ? kb % chunk_kb : 0;
+          if (by_block && in_chunk == 0 && !take_acc(d_tmem)) {
+            ok = false;
+            break;
           }
           if (!mbar_wait_cluster(&full[stage], phase, wd)) {
             ok = false;
@@ -212,21 +251,46 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t b_base = a_base + G::A_BYTES;
+          const bool last_kb = kb == p.k_blocks - 1;
+          if (by_block) {
 #pragma unroll
-          for (int kk = 0; kk < G::K_STEPS; ++kk) {
-            const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
-            mma_tf32_pair(d_tmem, ad, bd, p.idesc, (in_chunk | kk) != 0);
+            for (int kk = 0; kk < G::K_STEPS; ++kk) {
+              const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+              const uint32_t accumulate = (in_chunk | kk) != 0;
+              if (F16ACC)
+                mma_f16_pair(d_tmem, ad, bd, p.idesc, accumulate);
+              else
+                mma_tf32_pair(d_tmem, ad, bd, p.idesc, accumulate);
+            }
+            if (in_chunk == chunk_kb - 1 || last_kb) hand_over();
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < G::K_STEPS; ++kk) {
+              const bool fresh = left == 0;
+              if (fresh) {
+                if (!take_acc(d_tmem)) {
+                  ok = false;
+                  break;
+                }
+                left = chunk;
+              }
+              const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+              if (F16ACC)
+                mma_f16_pair(d_tmem, ad, bd, p.idesc, fresh ? 0u : 1u);
+              else
+                mma_tf32_pair(d_tmem, ad, bd, p.idesc, fresh ? 0u : 1u);
+              if (--left == 0 || (last_kb && kk == G::K_STEPS - 1)) {
+                hand_over();
+                left = 0;
+              }
+            }
           }
           mma_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1;
-          }
-          if (in_chunk == chunk - 1 || kb == p.k_blocks - 1) {  // chunk done: hand it over
-            mma_commit_pair_multicast(&tmem_full[acc], 0x3);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
           }
         }
       }
@@ -241,12 +305,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const int half = e >> 2;  // which 128 columns of the tile
     uint8_t *sb = smem + G::EPI_OFFSET + e * kStoreBufBytes;
     uint32_t acc = 0, acc_phase = 0;
-    const int chunks = (p.k_blocks + chunk - 1) / chunk;
+    const int chunks = (p.k_blocks * G::K_STEPS + chunk - 1) / chunk;
     bool ok = true;
     for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
-      float sum[G::COLS];
+      // The tile's running sums start at zero once: fp32 values (exact mode) or fp16 pairs
+      // (fp16 accumulator; +0 is the all-zero bit pattern).
+      float sum[F16ACC ? 1 : G::COLS];
+      __half2 hsum[F16ACC ? G::COLS / 2 : 1];
+      if (F16ACC) {
 #pragma unroll
-      for (int j = 0; j < G::COLS; ++j) sum[j] = 0.0f;  // the tile's sum starts at zero once
+        for (int j = 0; j < G::COLS / 2; ++j) hsum[j] = __floats2half2_rn(0.0f, 0.0f);
+      } else {
+#pragma unroll
+        for (int j = 0; j < G::COLS; ++j) sum[j] = 0.0f;
+      }
       for (int c = 0; c < chunks; ++c) {
         bool got = mbar_wait_cluster_inline(&tmem_full[acc], acc_phase, wd);
         got = __all_sync(0xffffffffu, got);
@@ -262,8 +334,17 @@ __global__ void __launch_bounds__(kXThreads, 1)
           uint32_t r[32];
           tmem_ld_32x32b_x32(t + q * 32, r);
           tmem_wait_ld();
+          if (F16ACC) {
+            // partial = fp16(chunk dot); acc = fp16(acc + partial)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum[q * 32 + j] += __uint_as_float(r[j]);
+            for (int j = 0; j < 16; ++j)
+              hsum[q * 16 + j] = __hadd2(
+                  hsum[q * 16 + j],
+                  __floats2half2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum[q * 32 + j] += __uint_as_float(r[j]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -276,21 +357,16 @@ __global__ void __launch_bounds__(kXThreads, 1)
       tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
       const int row0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM + quarter * 32;
       const int col0 = pn * G::BN + half * G::COLS;
-      if (p.tma_store) {
-        if (p.out_dtype == GEMM_BF16)
-          store_regs_tma<GEMM_BF16>(sum, &tmC, sb, lane, row0, col0, p.M, p.N);
-        else if (p.out_dtype == GEMM_F16)
-          store_regs_tma<GEMM_F16>(sum, &tmC, sb, lane, row0, col0, p.M, p.N);
-        else
-          store_regs_tma<GEMM_F32>(sum, &tmC, sb, lane, row0, col0, p.M, p.N);
-      } else {
-        if (p.out_dtype == GEMM_BF16)
-          store_regs_direct<GEMM_BF16>(sum, p, row0 + lane, col0);
-        else if (p.out_dtype == GEMM_F16)
-          store_regs_direct<GEMM_F16>(sum, p, row0 + lane, col0);
-        else
-          store_regs_direct<GEMM_F32>(sum, p, row0 + lane, col0);
-      }
+      float out[kXCols];
+#pragma unroll
+      for (int j = 0; j < kXCols; ++j)
+        out[j] = F16ACC ? (j % 2 ? __high2float(hsum[j / 2]) : __low2float(hsum[j / 2])) : sum[j];
+      if (p.out_dtype == GEMM_BF16)
+        store_regs<GEMM_BF16>(out, &tmC, sb, p, lane, row0, col0);
+      else if (p.out_dtype == GEMM_F16)
+        store_regs<GEMM_F16>(out, &tmC, sb, p, lane, row0, col0);
+      else
+        store_regs<GEMM_F32>(out, &tmC, sb, p, lane, row0, col0);
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -310,9 +386,24 @@ __global__ void __launch_bounds__(kXThreads, 1)
   }
 }
 
-}  // namespace
+template <bool F16ACC>
+cudaLaunchConfig_t chunk_config(int grid, cudaStream_t s, cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kXThreads, 1, 1);
+  cfg.dynamicSmemBytes = CfgX<F16ACC>::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
 
-int tc_exact_max_active_clusters() {
+template <bool F16ACC>
+int max_active_clusters() {
   static int cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -320,24 +411,15 @@ int tc_exact_max_active_clusters() {
     return 0;
   }
   if (cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(tc_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           CfgX::SMEM_BYTES) != cudaSuccess) {
+  if (cudaFuncSetAttribute(tc_chunk_kernel<F16ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           CfgX<F16ACC>::SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kXThreads, 1, 1);
-  cfg.dynamicSmemBytes = CfgX::SMEM_BYTES;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = chunk_config<F16ACC>(2, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_exact_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_chunk_kernel<F16ACC>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -345,24 +427,26 @@ int tc_exact_max_active_clusters() {
   return n;
 }
 
-cudaError_t tc_exact_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                            const TcParams &p, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(tc_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       CfgX::SMEM_BYTES);
+template <bool F16ACC>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                   const TcParams &p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(
+      tc_chunk_kernel<F16ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgX<F16ACC>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kXThreads, 1, 1);
-  cfg.dynamicSmemBytes = CfgX::SMEM_BYTES;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_exact_kernel, tmA, tmB, tmC, p);
+  cudaLaunchConfig_t cfg = chunk_config<F16ACC>(grid, s, attr);
+  return cudaLaunchKernelEx(&cfg, tc_chunk_kernel<F16ACC>, tmA, tmB, tmC, p);
+}
+
+}  // namespace
+
+int tc_chunk_max_active_clusters(bool f16acc) {
+  return f16acc ? max_active_clusters<true>() : max_active_clusters<false>();
+}
+
+cudaError_t tc_chunk_launch(bool f16acc, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                            const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
+  return f16acc ? launch<true>(tmA, tmB, tmC, p, grid, s) : launch<false>(tmA, tmB, tmC, p, grid, s);
 }
 
 }  // namespace gemm_gb300

@@ -40,8 +40,17 @@
  * GEMM_PREC_EXACT_FP32 keeps fp32 accuracy (max |err| <= 1e-6 * sum_k |a_ik b_kj|
  * on the library's tests): each operand is split into two tf32 parts and the
  * three significant partial products run on the tensor cores, accumulating in
- * fp32 (tiny problems use fp32 fused multiply-adds). 16-bit inputs accept only
- * GEMM_PREC_DEFAULT.
+ * fp32 (tiny problems use fp32 fused multiply-adds). 16-bit inputs accept
+ * GEMM_PREC_DEFAULT (fp32 accumulator) and, for fp16 inputs only,
+ * GEMM_PREC_F16_ACC: the fp16 accumulator of "Chapter 13: The Blocked Matmul
+ * Kernel", section 13.3 (Worked Example 13.3.1), kept to show what it costs. The
+ * running total is an fp16 value that starts at +0; for every chunk of
+ * GEMM_OPT_ACC_CHUNK consecutive K indices (from k = 0; default 16) the chunk's dot
+ * product is formed in fp32, rounded to fp16, and added to the running total with
+ * an fp16 round-to-nearest-even add; the total is then converted to out_dtype.
+ * Chunks that are multiples of 16 run on the tensor cores (each chunk's fp32 dot is
+ * one or more tcgen05.mma.kind::f16 into a fresh TMEM accumulator); other
+ * multiples of 8 (the pages' BLOCK_K = 8) run on fp32 fused multiply-adds.
  *
  * Errors: checks on the host return a status and launch nothing. Work is
  * asynchronous on the given stream, so a GEMM_OK return means "launched";
@@ -77,7 +86,8 @@ typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2 } gemm_dtype_t;
 typedef enum {
   GEMM_PREC_DEFAULT = 0,   /* exact fp32 for fp32 inputs; the only mode for 16-bit inputs */
   GEMM_PREC_TF32 = 1,      /* fp32 inputs on the tf32 tensor-core path */
-  GEMM_PREC_EXACT_FP32 = 2 /* fp32 inputs at fp32 accuracy (split-tf32 tensor cores) */
+  GEMM_PREC_EXACT_FP32 = 2, /* fp32 inputs at fp32 accuracy (split-tf32 tensor cores) */
+  GEMM_PREC_F16_ACC = 3     /* fp16 inputs, fp16 accumulator rounded every K-chunk */
 } gemm_precision_t;
 
 typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
@@ -173,10 +183,12 @@ typedef enum {
                                    (fixed-order reduction, handle-owned workspace):
                                    0 when it pays (>= 2 whole rounds first, >= 64 K-blocks),
                                    1 never, 2 whenever the schedule allows */
-  GEMM_OPT_HOST_PANEL = 10      /* gemm_run_host: rows of A and columns of B per pipelined
+  GEMM_OPT_HOST_PANEL = 10,     /* gemm_run_host: rows of A and columns of B per pipelined
                                    copy panel, a multiple of 256 (0 = auto: about 1/6 of the
                                    extent, >= 1024; widened to keep <= 24 such panels); the
                                    last two panels' worth is cut in halves down to 256 */
+  GEMM_OPT_ACC_CHUNK = 11       /* GEMM_PREC_F16_ACC: K indices per fp16 rounding of the
+                                   running total, a multiple of 8 (0 = default 16) */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
@@ -192,8 +204,10 @@ typedef enum {
   GEMM_PATH_ZERO_FILL = 1, /* K == 0: C is set to zero */
   GEMM_PATH_TCGEN05 = 2,   /* TMA + mbarrier pipeline + tcgen05.mma, TMEM accumulator */
   GEMM_PATH_FMA = 3,       /* fp32 fused multiply-add tiles (exact fp32, tiny problems) */
-  GEMM_PATH_TCGEN05_3XTF32 = 4 /* exact fp32 on the tensor cores: operands split into tf32
-                                  hi/lo parts, three products in one fp32 accumulator */
+  GEMM_PATH_TCGEN05_3XTF32 = 4, /* exact fp32 on the tensor cores: operands split into tf32
+                                   hi/lo parts, three products in one fp32 accumulator */
+  GEMM_PATH_TCGEN05_F16ACC = 5   /* fp16 accumulator on the tensor cores: each K-chunk's
+                                   fp32 dot from TMEM is rounded into an fp16 running total */
 } gemm_path_t;
 
 typedef struct {

@@ -145,6 +145,23 @@ def test_plan_fp32_modes():
     assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (4, 4, 4)
 
 
+def test_plan_fp16_accumulator():
+    # Section 13.3's fp16 accumulator: chunks of one 16-long MMA on the tensor cores (CTA
+    # pairs, 256 x 256 tiles); a row-major B is transposed into K-major form, since the
+    # chunked kernel reads K-major operands only.
+    a, b = t((4096, 1024), torch.float16), t((1024, 4096), torch.float16)
+    p = g.plan(a, b, precision="f16acc", sm_count=148)
+    assert p["path"] == "tcgen05_f16acc" and p["cta_pair"] == 1
+    assert (p["tile_m"], p["tile_n"], p["tile_k"], p["k_iters"]) == (256, 256, 64, 16)
+    assert p["stage_a"] == 0 and p["stage_b"] == 1 and p["b_mn_major"] == 0
+    assert p["split_tiles"] == 0
+    p = g.plan(a, t((4096, 1024), torch.float16).t(), precision="f16acc")
+    assert p["stage_b"] == 0
+    # the pages' 4 x 1024 @ 1024 x 4 example is tiny but keeps the tensor-core kernel
+    p = g.plan(t((4, 1024), torch.float16), t((1024, 4), torch.float16), precision="f16acc")
+    assert p["path"] == "tcgen05_f16acc"
+
+
 def test_plan_degenerate_shapes():
     assert g.plan(t((0, 5), torch.float16), t((5, 7), torch.float16))["path"] == "none"
     assert g.plan(t((5, 3), torch.float16), t((3, 0), torch.float16))["path"] == "none"
@@ -170,6 +187,10 @@ def test_plan_rejects_bad_arguments(L):
     assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, in_dt=7) == 1
     assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, al=3) == 1
     assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, prec=1) == 2  # tf32 with fp16 in
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, prec=3) == 0  # fp16 acc, fp16 in
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, prec=3, in_dt=2) == 2  # bf16 in
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, prec=3, in_dt=0) == 2  # fp32 in
+    assert plan_code(L, 16, 16, 16, A, 16, B, 16, C, 16, prec=4) == 1  # unknown mode
     assert plan_code(L, 16, 16, 16, A + 1, 16, B, 16, C, 16) == 3      # odd fp16 address
     assert plan_code(L, 16, 16, 16, A, 16, B, 16, C + 2, 16) == 3      # fp32 C at 2 bytes
     assert plan_code(L, 16, 16, 16, A, 16, B, 16, A + 64, 16) == 1     # C overlaps A

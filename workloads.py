@@ -179,6 +179,14 @@ def bf16_square(n, seed=2, b_layout="col"):
     return Problem("bf16_%d^3" % n, A, B, "bf16", "default")
 
 
+def f16acc_square(n, seed=6):
+    """fp16 n^3 in the fp16-accumulator mode: A row-major, B column-major, entries
+    N(0,1) * 0.1 (the scale of the 13.3.1 example), fp16 out."""
+    A = make_operand(n, n, "f16", "row", 2 * seed, "normal", scale=0.1)
+    B = make_operand(n, n, "f16", "col", 2 * seed + 1, "normal", scale=0.1)
+    return Problem("f16acc_%d^3" % n, A, B, "f16", "f16acc")
+
+
 def fp32_square(n, precision, seed=3):
     """fp32 n^3 row-major, uniform[-1, 1], fp32 out, tf32 or exact mode."""
     A = make_operand(n, n, "f32", "row", 2 * seed)
