@@ -42,7 +42,8 @@ _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
-           "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments", "gemm_run_host")
+           "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments", "gemm_run_host",
+           "gemm_run_strided", "gemm_plan_strided")
 
 
 class GemmError(RuntimeError):
@@ -50,6 +51,14 @@ class GemmError(RuntimeError):
         self.code = code
         self.status = STATUS.get(code, str(code))
         super().__init__("%s%s (%s)" % (what + ": " if what else "", self.status, _strerror(code)))
+
+
+class StridedInfo(ctypes.Structure):
+    _fields_ = [("a_gathered", ctypes.c_int32), ("b_gathered", ctypes.c_int32),
+                ("c_mode", ctypes.c_int32), ("buffer_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class PlanInfo(ctypes.Structure):
@@ -95,6 +104,13 @@ def lib():
                 L.gemm_run_ex.restype = i32
                 L.gemm_run_host.argtypes = run_args + [i32, i32, vp]
                 L.gemm_run_host.restype = i32
+                strided = [vp, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, i32,
+                           i32, i32]
+                L.gemm_run_strided.argtypes = strided + [vp]
+                L.gemm_run_strided.restype = i32
+                L.gemm_plan_strided.argtypes = strided + [i32, ctypes.POINTER(PlanInfo),
+                                                          ctypes.POINTER(StridedInfo)]
+                L.gemm_plan_strided.restype = i32
                 L.gemm_get_status.argtypes = [vp, vp]
                 L.gemm_get_status.restype = i32
                 L.gemm_strerror.argtypes = [i32]
@@ -197,11 +213,14 @@ class Gemm:
                                  precision, a_layout, b_layout, ctypes.c_void_p(stream))
 
     def matmul(self, a, b, out=None, out_dtype=None, precision="default", stream=None):
-        """C = a @ b on the GPU; a is M x K, b is K x N (row- or column-major views)."""
+        """C = a @ b on the GPU; a is M x K, b is K x N, out M x N: any 2-D views (row- or
+        column-major views go through gemm_run_ex, others through gemm_run_strided)."""
         if a.dtype != b.dtype:
             raise TypeError("a and b must share a dtype")
         if not (a.is_cuda and b.is_cuda):
             raise ValueError("operands must be CUDA tensors (see matmul_host for host buffers)")
+        if a.dim() != 2 or b.dim() != 2:
+            raise ValueError("operands must be 2-D")
         M, K = a.shape
         K2, N = b.shape
         if K != K2:
@@ -210,18 +229,29 @@ class Gemm:
         if out is None:
             od = _TORCH_OF[_dtype_code(out_dtype)] if out_dtype is not None else a.dtype
             out = torch.empty((M, N), dtype=od, device=a.device)
-        if out.dim() != 2 or out.shape != (M, N) or (N > 1 and out.stride(1) != 1):
-            raise ValueError("out must be a row-major M x N tensor")
-        al, lda = operand_layout(a)
-        bl, ldb = operand_layout(b)
-        ldc = max(out.stride(0), N, 1)
+        if out.dim() != 2 or out.shape != (M, N):
+            raise ValueError("out must be an M x N tensor")
         s = torch.cuda.current_stream(a.device) if stream is None else stream
-        code = lib().gemm_run_ex(self._h, M, N, K, ctypes.c_void_p(a.data_ptr()), lda,
-                                 ctypes.c_void_p(b.data_ptr()), ldb,
-                                 ctypes.c_void_p(out.data_ptr()), ldc, in_dt,
-                                 _dtype_code(out.dtype), PREC[precision], al, bl,
-                                 ctypes.c_void_p(s.cuda_stream))
-        _check(code, "gemm_run_ex")
+        ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+        try:
+            al, lda = operand_layout(a)
+            bl, ldb = operand_layout(b)
+            row_c = (N <= 1 or out.stride(1) == 1) and (M <= 1 or out.stride(0) >= N)
+        except ValueError:
+            row_c = False
+        if row_c:
+            ldc = max(out.stride(0) if M > 1 else N, N, 1)
+            code = lib().gemm_run_ex(self._h, M, N, K, ptr(a), lda, ptr(b), ldb, ptr(out), ldc,
+                                     in_dt, _dtype_code(out.dtype), PREC[precision], al, bl,
+                                     ctypes.c_void_p(s.cuda_stream))
+            _check(code, "gemm_run_ex")
+        else:
+            code = lib().gemm_run_strided(self._h, M, N, K, ptr(a), a.stride(0), a.stride(1),
+                                          ptr(b), b.stride(0), b.stride(1), ptr(out),
+                                          out.stride(0), out.stride(1), in_dt,
+                                          _dtype_code(out.dtype), PREC[precision],
+                                          ctypes.c_void_p(s.cuda_stream))
+            _check(code, "gemm_run_strided")
         return out
 
     def matmul_host(self, a, b, out=None, out_dtype=None, precision="default", stream=None):
@@ -259,6 +289,27 @@ class Gemm:
         """The planner's decision for these operands (host-only, nothing launched)."""
         return plan(a, b, out=out, out_dtype=out_dtype, precision=precision,
                     sm_count=sm_count, handle=self)
+
+
+def plan_strided(a, b, out=None, out_dtype=None, precision="default", sm_count=148,
+                 handle=None):
+    """Host-only query of gemm_run_strided's decisions for these views (works without a
+    GPU): (plan dict, strided-info dict)."""
+    M, K = a.shape
+    N = b.shape[1]
+    od = _dtype_code(out_dtype) if out_dtype is not None else _dtype_code(a.dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=_TORCH_OF[od])
+    info, sinfo = PlanInfo(), StridedInfo()
+    h = handle.handle if handle is not None else None
+    code = lib().gemm_plan_strided(h, M, N, K, ctypes.c_void_p(a.data_ptr()), a.stride(0),
+                                   a.stride(1), ctypes.c_void_p(b.data_ptr()), b.stride(0),
+                                   b.stride(1), ctypes.c_void_p(out.data_ptr()), out.stride(0),
+                                   out.stride(1), _dtype_code(a.dtype), _dtype_code(out.dtype),
+                                   PREC[precision], sm_count, ctypes.byref(info),
+                                   ctypes.byref(sinfo))
+    _check(code, "gemm_plan_strided")
+    return info.as_dict(), sinfo.as_dict()
 
 
 def plan(a, b, out=None, out_dtype=None, precision="default", sm_count=148, handle=None,

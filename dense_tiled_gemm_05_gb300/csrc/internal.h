@@ -107,6 +107,11 @@ cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t
 cudaError_t split3_launch(const float *src, int64_t lds, bool k_contig, float *dst, int64_t ldd,
                           int64_t R, int64_t K, bool is_b, cudaStream_t s);
 
+// dst[i * d0 + j * d1] = src[i * s0 + j * s1] for i < n0, j < n1 (element strides; the
+// source's may be 0). esize is 2 or 4 bytes.
+cudaError_t strided_copy_launch(const void *src, int64_t s0, int64_t s1, void *dst, int64_t d0,
+                                int64_t d1, int64_t n0, int64_t n1, int esize, cudaStream_t s);
+
 // C[i, j] = 0 for i < M, j < N.
 cudaError_t zero_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, int out_dtype,
                              cudaStream_t s);

@@ -235,6 +235,46 @@ GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t 
                                  gemm_layout_t a_layout, gemm_layout_t b_layout,
                                  int32_t sm_count, gemm_plan_info_t *info);
 
+/* ------------------------------------------------------- six-stride interface */
+
+/* C = A @ B for any 2D views: element (i, k) of A is at A + i * stride_am + k * stride_ak,
+ * (k, j) of B at B + k * stride_bk + j * stride_bn, and (i, j) of C at
+ * C + i * stride_cm + j * stride_cn (strides in elements) -- the six strides the pages'
+ * host wrapper passes its kernel ("Chapter 13: The Blocked Matmul Kernel", section 13.4).
+ * A and B strides must be >= 0 (0 repeats a row or column: a broadcast view); C strides
+ * must be >= 1 along extents above 1, and no two elements of C may share an address; C may
+ * not overlap A or B. A view with a unit stride and a leading stride spanning its lines is
+ * read in place (the same path as gemm_run_ex); a column-major C is computed as
+ * C^T = B^T A^T in place; any other operand is first gathered into a handle-owned buffer
+ * (grown on demand) and any other C is written through a row-major temporary there. Same
+ * dtypes, precision modes, errors and stream semantics as gemm_run_ex. */
+GEMM_API gemm_status_t gemm_run_strided(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                        const void *A, int64_t stride_am, int64_t stride_ak,
+                                        const void *B, int64_t stride_bk, int64_t stride_bn,
+                                        void *C, int64_t stride_cm, int64_t stride_cn,
+                                        gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+                                        gemm_precision_t precision_mode, void *cuda_stream);
+
+typedef struct {
+  int32_t a_gathered;   /* 1 if A is gathered into the handle's buffer first */
+  int32_t b_gathered;   /* 1 if B is gathered */
+  int32_t c_mode;       /* 0: C written in place (row-major); 1: C column-major, written in
+                           place as C^T = B^T A^T; 2: through a row-major temporary */
+  int64_t buffer_bytes; /* handle buffer the call needs for gathers and the temporary */
+} gemm_strided_info_t;
+
+/* Host-only: how gemm_run_strided would run these arguments (`info` as gemm_plan fills
+ * it for the problem after gathering or transposition; either pointer may be NULL). Same
+ * checks and return codes as gemm_run_strided; h may be NULL (default options). */
+GEMM_API gemm_status_t gemm_plan_strided(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                         const void *A, int64_t stride_am, int64_t stride_ak,
+                                         const void *B, int64_t stride_bk, int64_t stride_bn,
+                                         void *C, int64_t stride_cm, int64_t stride_cn,
+                                         gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+                                         gemm_precision_t precision_mode, int32_t sm_count,
+                                         gemm_plan_info_t *info, gemm_strided_info_t *sinfo);
+
+
 /* One piece of a worker's share of the output tiles (see gemm_schedule_segments). */
 typedef struct {
   int32_t tile;      /* output tile index in the grouped raster order */
