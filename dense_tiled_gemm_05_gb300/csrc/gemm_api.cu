@@ -40,6 +40,7 @@ struct gemm_handle_s {
   int block_n = 0;   // 0 auto, else 128 or 256
   int exact_chunk = 0;  // 0 default
   int acc_chunk = 0;    // fp16-accumulator chunk in K elements, 0 default (16)
+  int stage_k = 0;      // 128-byte K-blocks per stage of the CTA-pair kernel, 0 auto
   int stream_k = 0;     // 0 auto (on), 1 off
   int host_panel = 0;  // gemm_run_host panel width (rows of A, columns of B), 0 auto
   // split-K workspace of the CTA-pair kernel: partial tiles and flags
@@ -138,7 +139,7 @@ struct Problem {
 
 struct Options {
   int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
-  int stream_k = 0, exact_chunk = 0, acc_chunk = 0;
+  int stream_k = 0, exact_chunk = 0, acc_chunk = 0, stage_k = 0;
 };
 
 // fp16-accumulator chunk (K elements per fp16 rounding of the running total) when the
@@ -371,10 +372,26 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
     pl.variant.block_n = 256;
   }
   const bool chunked = pl.variant.exact || pl.variant.f16acc;
+  // Two 128-byte K-blocks per stage (CTA-pair kernel, K-major 16-bit operands): each row
+  // of A and B is then fetched 256 contiguous bytes at a time. By default only for
+  // bandwidth-bound products (under ~256 flops per byte of A, B and C), where it measured
+  // +1.5 % on bf16 16384 x 128 x 8192; compute-bound ones keep the deeper ring of one
+  // K-block per stage (4096^3 lost 9 % with wide stages). A forced split-K keeps narrow
+  // K-blocks, the finer unit it shares out (one 256 x 256 x 8192 tile: 128 units for 76
+  // clusters rather than 64).
+  const bool wide_ok = pl.variant.pair && !chunked && es == 2 && !pl.a.mn_major && !pl.b.mn_major;
+  if (opt.stage_k == 2 && !wide_ok) return GEMM_ERR_UNSUPPORTED;
+  const double intensity = 2.0 * P.M * P.N * P.K /
+                           (es * (static_cast<double>(P.M) * P.K + static_cast<double>(P.K) * P.N) +
+                            static_cast<double>(os) * P.M * P.N);
+  pl.variant.kps =
+      opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < 256.0 && opt.stream_k != 2)
+          ? 2
+          : 1;
   I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : f16acc ? GEMM_PATH_TCGEN05_F16ACC : GEMM_PATH_TCGEN05;
   I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
   I.tile_n = pl.variant.block_n;
-  I.tile_k = 128 / es;
+  I.tile_k = pl.variant.kps * 128 / es;
   I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
   I.grid_n = (P.N + I.tile_n - 1) / I.tile_n;
   const int64_t k_total = split ? 3 * P.K : P.K;  // split operands concatenate 3 products
@@ -493,6 +510,7 @@ Options options_of(gemm_handle_t h) {
     o.stream_k = h->stream_k;
     o.exact_chunk = h->exact_chunk;
     o.acc_chunk = h->acc_chunk;
+    o.stage_k = h->stage_k;
   }
   return o;
 }
@@ -777,6 +795,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
     case GEMM_OPT_CTA_PAIR:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
+      return GEMM_OK;
+    case GEMM_OPT_STAGE_K:
+      if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
+      h->stage_k = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_ACC_CHUNK:
       if (v < 0 || v > (int64_t{1} << 20) || v % 8) return GEMM_ERR_INVALID_ARG;

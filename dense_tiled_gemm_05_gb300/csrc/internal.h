@@ -46,6 +46,8 @@ struct TcVariant {
   bool pair;   // CTA pair (cta_group::2): 256-row tiles over two SMs
   bool exact;   // exact-fp32 kernel on split operands (CTA pairs, chunked fp32 sums)
   bool f16acc;  // fp16-accumulator kernel (CTA pairs, chunk dots rounded into fp16 sums)
+  int kps = 1;  // CTA-pair kernel: 128-byte K-blocks per pipeline stage (1, or 2 for K-major
+                // 16-bit operands)
 };
 
 int tc_stages(const TcVariant &v);

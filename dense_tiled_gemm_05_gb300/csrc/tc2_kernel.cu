@@ -14,6 +14,10 @@
 //     barrier (the peer arrives remotely).
 // Each SM therefore streams half as much B per flop as the single-CTA 128 x 256 tile, and
 // each output tile needs half the L2 traffic per flop.
+//
+// A stage holds KPS consecutive 128-byte K-blocks of each K-major operand (KPS = 1 or 2):
+// with 2, every row of A and B is fetched 256 contiguous bytes at a time, which keeps more
+// of each DRAM page's bytes in one request stream when the product is bandwidth-bound.
 #include "tc_common.cuh"
 
 namespace gemm_gb300 {
@@ -21,20 +25,24 @@ namespace {
 
 using namespace tc;
 
-template <int ESIZE, bool A_MN, bool B_MN, int BN_>
+template <int ESIZE, bool A_MN, bool B_MN, int BN_, int KPS = 1>
 struct Cfg2 {
   static constexpr int BM = kTcBlockM;             // rows per CTA (256 per pair)
   static constexpr int BN = BN_;                   // columns per pair tile (256 or 128)
   static constexpr int BN_HALF = BN / 2;           // B columns loaded by each CTA
-  static constexpr int BK = kRowBytes / ESIZE;     // K elements per stage
+  static constexpr int BOX_K = kRowBytes / ESIZE;  // K elements per 128-byte K-block
+  static constexpr int BK = KPS * BOX_K;           // K elements per stage
   static constexpr int UMMA_K = 32 / ESIZE;        // K elements per tcgen05.mma
   static constexpr int K_STEPS = BK / UMMA_K;
+  static constexpr int BOX_STEPS = BOX_K / UMMA_K;  // MMAs per K-block
   static constexpr int PANEL = kRowBytes / ESIZE;  // M/N elements per 128-byte row (MN-major)
   static constexpr int PANEL_BYTES = BK * kRowBytes;
   static constexpr int A_BYTES = BM * BK * ESIZE;
   static constexpr int B_BYTES = BN_HALF * BK * ESIZE;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
-  static constexpr int STAGES = BN >= 256 ? 6 : 8;
+  static constexpr int A_BOX_BYTES = BM * kRowBytes;       // one K-block of A
+  static constexpr int B_BOX_BYTES = BN_HALF * kRowBytes;  // one K-block of B
+  static constexpr int STAGES = (BN >= 256 ? 6 : 8) / KPS;
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * 2 * kStoreBufBytes;
   static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
@@ -46,15 +54,16 @@ struct Cfg2 {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(kEpiWarps * OWNER_SLICE <= STAGES * STAGE_BYTES, "owner slices fit the stages");
   static_assert(BN * 32 * 4 <= OWNER_SLICE, "a warp's partial rows fit its slice");
+  static_assert(KPS == 1 || (!A_MN && !B_MN), "wide stages for K-major operands only");
 };
 
-template <int ESIZE, bool A_MN, bool B_MN, int BN>
+template <int ESIZE, bool A_MN, bool B_MN, int BN, int KPS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmP, const TcParams p) {
-  using G = Cfg2<ESIZE, A_MN, B_MN, BN>;
+  using G = Cfg2<ESIZE, A_MN, B_MN, BN, KPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -130,14 +139,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < G::BM / G::PANEL; ++q)
               tma_load_2d_pair(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0);
           } else {
-            tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+#pragma unroll
+            for (int j = 0; j < KPS; ++j)
+              tma_load_2d_pair(a_dst + j * G::A_BOX_BYTES, &tmA, fb, k0 + j * G::BOX_K, m0);
           }
           if (B_MN) {
 #pragma unroll
             for (int q = 0; q < G::BN_HALF / G::PANEL; ++q)
               tma_load_2d_pair(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0);
           } else {
-            tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
+#pragma unroll
+            for (int j = 0; j < KPS; ++j)
+              tma_load_2d_pair(b_dst + j * G::B_BOX_BYTES, &tmB, fb, k0 + j * G::BOX_K, n0);
           }
           if (++stage == G::STAGES) {
             stage = 0;
@@ -168,12 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_base = a_base + G::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < G::K_STEPS; ++kk) {
+            // K-major: K-block kk / BOX_STEPS of the stage, 32 bytes per MMA inside it
+            const uint32_t a_k = (kk / G::BOX_STEPS) * G::A_BOX_BYTES + (kk % G::BOX_STEPS) * 32;
+            const uint32_t b_k = (kk / G::BOX_STEPS) * G::B_BOX_BYTES + (kk % G::BOX_STEPS) * 32;
             const uint64_t ad =
                 A_MN ? sdesc_sw128(a_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
-                     : sdesc_sw128(a_base + kk * 32, 16, 1024);
+                     : sdesc_sw128(a_base + a_k, 16, 1024);
             const uint64_t bd =
                 B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
-                     : sdesc_sw128(b_base + kk * 32, 16, 1024);
+                     : sdesc_sw128(b_base + b_k, 16, 1024);
             const uint32_t accumulate = (kb != seg.kb_begin) || kk != 0;
             if (ESIZE == 2)
               mma_f16_pair(d_tmem, ad, bd, p.idesc, accumulate);
@@ -298,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int ESIZE, bool A_MN, bool B_MN, int BN>
+template <int ESIZE, bool A_MN, bool B_MN, int BN, int KPS = 1>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const CUtensorMap &tmP, const TcParams &p, int grid, cudaStream_t s) {
-  using G = Cfg2<ESIZE, A_MN, B_MN, BN>;
-  auto kernel = tc2_gemm_kernel<ESIZE, A_MN, B_MN, BN>;
+  using G = Cfg2<ESIZE, A_MN, B_MN, BN, KPS>;
+  auto kernel = tc2_gemm_kernel<ESIZE, A_MN, B_MN, BN, KPS>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -341,8 +357,8 @@ int tc2_max_active_clusters() {
     return 0;
   }
   if (cached[dev] > 0) return cached[dev];
-  using G = Cfg2<2, false, false, 256>;
-  auto kernel = tc2_gemm_kernel<2, false, false, 256>;
+  using G = Cfg2<2, false, false, 256, 1>;
+  auto kernel = tc2_gemm_kernel<2, false, false, 256, 1>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -372,6 +388,11 @@ cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtenso
                        const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p, int grid,
                        cudaStream_t s) {
   // tf32 operands are always K-major (MN-major fp32 operands are staged transposed).
+  if (v.kps == 2 && v.esize == 2 && !v.a_mn && !v.b_mn) {
+    if (v.block_n == 256) return launch_pair<2, false, false, 256, 2>(tmA, tmB, tmC, tmP, p, grid, s);
+    if (v.block_n == 128) return launch_pair<2, false, false, 128, 2>(tmA, tmB, tmC, tmP, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
   if (v.esize == 2 && v.block_n == 256)
     return launch_pair_majors<2, 256>(v, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.esize == 2 && v.block_n == 128)

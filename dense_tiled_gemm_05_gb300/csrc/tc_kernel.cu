@@ -266,7 +266,7 @@ cudaError_t launch_majors(const TcVariant &v, const CUtensorMap &tmA, const CUte
 }  // namespace
 
 int tc_stages(const TcVariant &v) {
-  if (v.pair) return v.block_n >= 256 ? 6 : 8;
+  if (v.pair) return (v.block_n >= 256 ? 6 : 8) / v.kps;
   return v.block_n >= 256 ? 4 : 6;
 }
 

@@ -187,8 +187,11 @@ typedef enum {
                                    copy panel, a multiple of 256 (0 = auto: about 1/6 of the
                                    extent, >= 1024; widened to keep <= 24 such panels); the
                                    last two panels' worth is cut in halves down to 256 */
-  GEMM_OPT_ACC_CHUNK = 11       /* GEMM_PREC_F16_ACC: K indices per fp16 rounding of the
+  GEMM_OPT_ACC_CHUNK = 11,      /* GEMM_PREC_F16_ACC: K indices per fp16 rounding of the
                                    running total, a multiple of 8 (0 = default 16) */
+  GEMM_OPT_STAGE_K = 12         /* 128-byte K-blocks per pipeline stage of the CTA-pair
+                                   kernel: 0 auto, 1, or 2 (K-major 16-bit operands only;
+                                   otherwise GEMM_ERR_UNSUPPORTED at run time) */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */

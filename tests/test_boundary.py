@@ -86,9 +86,12 @@ def test_plan_bf16_square_is_tcgen05_k_major():
     p = g.plan(t((8192, 8192), torch.bfloat16), t((8192, 8192), torch.bfloat16, "col"),
                sm_count=148)
     assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 256, 32, 32)
+    assert (p["tile_k"], p["stages"]) == (64, 6)  # compute-bound: one K-block per stage
     p = g.plan(t((16384, 8192), torch.bfloat16), t((8192, 128), torch.bfloat16, "col"),
                sm_count=148)
     assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 128, 64, 1)
+    # bandwidth-bound (125 flops per byte): two 128-byte K-blocks per stage, half the stages
+    assert (p["tile_k"], p["k_iters"], p["stages"]) == (128, 64, 4)
     # One 128-row tile of M: single-CTA tiles.
     p = g.plan(t((128, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
                sm_count=148)

@@ -383,3 +383,27 @@ def test_bf16_skinny(h):
     assert err <= tolerance(p), err
     s_err, tol = check_sums(p, c)
     assert s_err <= tol, s_err
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("stream_k", [1, 2])
+def test_wide_stages_integer_exact(block_n, stream_k):
+    # Two 128-byte K-blocks per pipeline stage: K = 64 (the second block entirely past K,
+    # read as zeros), ragged K, and K long enough for split-K pieces of 128-wide K-blocks.
+    import dense_tiled_gemm_05_gb300 as g
+    h2 = g.Gemm(0)
+    h2.set_option("stage_k", 2)
+    h2.set_option("block_n", block_n)
+    h2.set_option("stream_k", stream_k)
+    for n, (M, N, K) in enumerate([(300, 257, 64), (513, 300, 1025), (1030, 530, 1200),
+                                   (256, 256, 8192)]):
+        p = W.integer_problem(M, N, K, "bf16", seed=40 + n, b_layout="col")
+        plan = h2.plan(to_device(p.A), to_device(p.B), out_dtype="f32")
+        assert plan["tile_k"] == 128 and plan["stages"] == (3 if block_n == 256 else 4)
+        c = run_gpu(h2, p)
+        assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    # operands the wide stages do not take are refused, not silently narrowed
+    p = W.integer_problem(300, 200, 64, "bf16", seed=49)  # row-major B: MN-major
+    with pytest.raises(g.GemmError):
+        run_gpu(h2, p)
+    h2.close()
