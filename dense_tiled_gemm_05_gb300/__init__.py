@@ -43,7 +43,7 @@ _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
            "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments", "gemm_run_host",
-           "gemm_run_strided", "gemm_plan_strided")
+           "gemm_run_strided", "gemm_plan_strided", "gemm_tune", "gemm_tune_clear")
 
 
 class GemmError(RuntimeError):
@@ -51,6 +51,16 @@ class GemmError(RuntimeError):
         self.code = code
         self.status = STATUS.get(code, str(code))
         super().__init__("%s%s (%s)" % (what + ": " if what else "", self.status, _strerror(code)))
+
+
+class TuneResult(ctypes.Structure):
+    _fields_ = [("cta_pair", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("stream_k", ctypes.c_int32), ("stage_k", ctypes.c_int32),
+                ("group_m", ctypes.c_int32), ("candidates", ctypes.c_int32),
+                ("best_us", ctypes.c_float), ("default_us", ctypes.c_float)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class StridedInfo(ctypes.Structure):
@@ -111,6 +121,10 @@ def lib():
                 L.gemm_plan_strided.argtypes = strided + [i32, ctypes.POINTER(PlanInfo),
                                                           ctypes.POINTER(StridedInfo)]
                 L.gemm_plan_strided.restype = i32
+                L.gemm_tune.argtypes = run_args + [i32, i32, vp, i32, ctypes.POINTER(TuneResult)]
+                L.gemm_tune.restype = i32
+                L.gemm_tune_clear.argtypes = [vp]
+                L.gemm_tune_clear.restype = i32
                 L.gemm_get_status.argtypes = [vp, vp]
                 L.gemm_get_status.restype = i32
                 L.gemm_strerror.argtypes = [i32]
@@ -254,6 +268,30 @@ class Gemm:
             _check(code, "gemm_run_strided")
         return out
 
+    def tune(self, a, b, out=None, out_dtype=None, precision="default", iters=5, stream=None):
+        """Time the tile-shape configurations for this problem (row- or column-major CUDA
+        views) and keep the fastest for its signature on this handle; returns the choice
+        as a dict (see gemm_tune). C is written."""
+        M, K = a.shape
+        N = b.shape[1]
+        if out is None:
+            od = _TORCH_OF[_dtype_code(out_dtype)] if out_dtype is not None else a.dtype
+            out = torch.empty((M, N), dtype=od, device=a.device)
+        al, lda = operand_layout(a)
+        bl, ldb = operand_layout(b)
+        s = torch.cuda.current_stream(a.device) if stream is None else stream
+        r = TuneResult()
+        code = lib().gemm_tune(self._h, M, N, K, ctypes.c_void_p(a.data_ptr()), lda,
+                               ctypes.c_void_p(b.data_ptr()), ldb, ctypes.c_void_p(out.data_ptr()),
+                               max(out.stride(0), N, 1), _dtype_code(a.dtype),
+                               _dtype_code(out.dtype), PREC[precision], al, bl,
+                               ctypes.c_void_p(s.cuda_stream), int(iters), ctypes.byref(r))
+        _check(code, "gemm_tune")
+        return r.as_dict()
+
+    def tune_clear(self):
+        _check(lib().gemm_tune_clear(self._h), "gemm_tune_clear")
+
     def matmul_host(self, a, b, out=None, out_dtype=None, precision="default", stream=None):
         """C = a @ b for HOST tensors through gemm_run_host: the library copies A and B to the
         GPU and C back, overlapping the copies of one row panel with the product of another.
@@ -286,7 +324,10 @@ class Gemm:
         return out
 
     def plan(self, a, b, out=None, out_dtype=None, precision="default", sm_count=None):
-        """The planner's decision for these operands (host-only, nothing launched)."""
+        """The planner's decision for these operands (host-only, nothing launched); by
+        default for this handle's device's SM count."""
+        if sm_count is None:
+            sm_count = torch.cuda.get_device_properties(self.device).multi_processor_count
         return plan(a, b, out=out, out_dtype=out_dtype, precision=precision,
                     sm_count=sm_count, handle=self)
 

@@ -15,12 +15,20 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "gemm.h"
 #include "internal.h"
 #include "sk_schedule.h"
 
 using namespace gemm_gb300;
+
+// A tuned choice of the tile-shape options for one problem signature (gemm_tune).
+struct TuneEntry {
+  int64_t M, N, K;
+  int in_dtype, out_dtype, precision, a_layout, b_layout;
+  gemm_tune_result_t choice;
+};
 
 struct gemm_handle_s {
   int device = 0;
@@ -32,7 +40,7 @@ struct gemm_handle_s {
   // options
   uint64_t timeout_us = 2000000;
   int force_path = 0;
-  int group_m = 8;
+  int group_m = 16;  // gemm_tune chose 16 on bf16 4096^3-8192^3 and tf32 4096^3 (+1-2 %)
   int max_ctas = 0;
   int stall_producer = 0;
   int force_staging = 0;
@@ -57,6 +65,7 @@ struct gemm_handle_s {
   cudaStream_t hp_stream[3] = {nullptr, nullptr, nullptr};  // H2D, compute, D2H
   cudaEvent_t hp_event[2 + 4 * kMaxPanels] = {};
   bool hp_ready = false;
+  std::vector<TuneEntry> tuned;  // gemm_tune's choices, by problem signature
 };
 
 namespace {
@@ -138,7 +147,7 @@ struct Problem {
 };
 
 struct Options {
-  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
+  int force_path = 0, group_m = 16, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
   int stream_k = 0, exact_chunk = 0, acc_chunk = 0, stage_k = 0;
 };
 
@@ -172,6 +181,8 @@ struct Plan {
   int fma_tile;
   int chunk_steps;    // chunked tensor-core kernel: MMA instructions per TMEM partial
   int64_t acc_chunk;  // fp16 accumulator: K elements per rounding (0: fp32 accumulator)
+  int group_m;        // raster group height (tile rows)
+  int stream_k;       // GEMM_OPT_STREAM_K value the plan was made with
 };
 
 gemm_status_t check_args(const Problem &P) {
@@ -306,6 +317,8 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   gemm_status_t st = check_args(P);
   if (st != GEMM_OK) return st;
   Plan pl{};
+  pl.group_m = opt.group_m;
+  pl.stream_k = opt.stream_k;
   gemm_plan_info_t &I = pl.info;
   if (P.M == 0 || P.N == 0) {
     I.path = GEMM_PATH_NONE;
@@ -358,9 +371,18 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   pl.variant.esize = es;
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
+  // Flops per byte of A, B and C: under ~256 the product is bandwidth-bound on GB300.
+  const double intensity = 2.0 * P.M * P.N * P.K /
+                           (es * (static_cast<double>(P.M) * P.K + static_cast<double>(P.K) * P.N) +
+                            static_cast<double>(os) * P.M * P.N);
   // CTA pairs (256-row tiles on two SMs) halve the shared-memory and L2 traffic per
-  // flop; a problem no taller than one 128-row tile keeps single-CTA tiles.
-  pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM);
+  // flop; a problem no taller than one 128-row tile keeps single-CTA tiles, and so does a
+  // compute-bound one whose 128 x 256 single-CTA tiles all run at once (one round on the
+  // SMs), where the pair's cross-SM handshakes cost more than they save (bf16 2048^3:
+  // 16.6 against 18.7 us). Bandwidth-bound ones keep pairs, for their wide stages.
+  const int64_t single_tiles = ((P.M + kTcBlockM - 1) / kTcBlockM) * ((P.N + 255) / 256);
+  const bool one_round = single_tiles <= sm_count && intensity >= 256.0;
+  pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM && !one_round);
   pl.variant.block_n =
       opt.block_n ? opt.block_n
                   : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
@@ -381,9 +403,6 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // clusters rather than 64).
   const bool wide_ok = pl.variant.pair && !chunked && es == 2 && !pl.a.mn_major && !pl.b.mn_major;
   if (opt.stage_k == 2 && !wide_ok) return GEMM_ERR_UNSUPPORTED;
-  const double intensity = 2.0 * P.M * P.N * P.K /
-                           (es * (static_cast<double>(P.M) * P.K + static_cast<double>(P.K) * P.N) +
-                            static_cast<double>(os) * P.M * P.N);
   pl.variant.kps =
       opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < 256.0 && opt.stream_k != 2)
           ? 2
@@ -511,6 +530,30 @@ Options options_of(gemm_handle_t h) {
     o.exact_chunk = h->exact_chunk;
     o.acc_chunk = h->acc_chunk;
     o.stage_k = h->stage_k;
+  }
+  return o;
+}
+
+const TuneEntry *find_tuned(gemm_handle_t h, const Problem &P) {
+  if (!h) return nullptr;
+  for (const TuneEntry &t : h->tuned)
+    if (t.M == P.M && t.N == P.N && t.K == P.K && t.in_dtype == P.in_dtype &&
+        t.out_dtype == P.out_dtype && t.precision == P.precision && t.a_layout == P.a_layout &&
+        t.b_layout == P.b_layout)
+      return &t;
+  return nullptr;
+}
+
+// The handle's options, with the tile-shape options gemm_tune chose for this problem
+// signature (if it was tuned) in place of the handle's.
+Options options_for(gemm_handle_t h, const Problem &P) {
+  Options o = options_of(h);
+  if (const TuneEntry *t = find_tuned(h, P)) {
+    o.cta_pair = t->choice.cta_pair;
+    o.block_n = t->choice.block_n;
+    o.stream_k = t->choice.stream_k;
+    o.stage_k = t->choice.stage_k;
+    o.group_m = t->choice.group_m;
   }
   return o;
 }
@@ -673,9 +716,9 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   }
   SplitK sk;
   sk.h = h;
-  sk.mode = h->stream_k;
+  sk.mode = pl.stream_k;
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
-                 h->group_m, h->stall_producer ? kDebugStallProducer : 0, sk, s);
+                 pl.group_m, h->stall_producer ? kDebugStallProducer : 0, sk, s);
   if (st != GEMM_OK) return st;
   h->launches += 1;
   return GEMM_OK;
@@ -839,7 +882,7 @@ GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t 
   const Problem P{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
                   b_layout};
   Plan pl;
-  gemm_status_t st = make_plan(P, options_of(h), sm_count, &pl);
+  gemm_status_t st = make_plan(P, options_for(h, P), sm_count, &pl);
   if (st == GEMM_OK) *info = pl.info;
   return st;
 }
@@ -854,11 +897,126 @@ GEMM_API gemm_status_t gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_
   const Problem P{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
                   b_layout};
   Plan pl;
-  gemm_status_t st = make_plan(P, options_of(h), h->sm_count, &pl);
+  gemm_status_t st = make_plan(P, options_for(h, P), h->sm_count, &pl);
   if (st != GEMM_OK) return st;
   DeviceGuard g(h->device);
   if (!g.ok) return GEMM_ERR_CUDA;
   return execute(h, P, pl, static_cast<cudaStream_t>(cuda_stream));
+}
+
+// ------------------------------------------------------------------ tuning
+//
+// The pages choose BLOCK_M/N/K per call; here the planner picks the tile shape, the
+// split-K share, the stage width and the raster group by fixed rules. gemm_tune measures
+// the alternatives for one problem on the device and keeps the fastest for its signature.
+
+namespace {
+
+gemm_tune_result_t choice_of(const Options &o, const Plan &pl) {
+  gemm_tune_result_t c{};
+  c.cta_pair = pl.variant.pair ? 2 : 1;
+  c.block_n = pl.variant.block_n;
+  c.stream_k = o.stream_k;
+  c.stage_k = pl.variant.kps;
+  c.group_m = o.group_m;
+  return c;
+}
+
+}  // namespace
+
+GEMM_API gemm_status_t gemm_tune(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+                                 int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
+                                 gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+                                 gemm_precision_t precision_mode, gemm_layout_t a_layout,
+                                 gemm_layout_t b_layout, void *cuda_stream, int32_t iters,
+                                 gemm_tune_result_t *result) {
+  if (!h || iters < 1 || iters > 1000) return GEMM_ERR_INVALID_ARG;
+  const Problem P{M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, precision_mode, a_layout,
+                  b_layout};
+  const Options base = options_of(h);
+  Plan pl0;
+  gemm_status_t st = make_plan(P, base, h->sm_count, &pl0);
+  if (st != GEMM_OK) return st;
+  DeviceGuard g(h->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  // Candidates: the untuned plan first, then every combination of the tile-shape options
+  // that plans to a distinct configuration.
+  struct Cand {
+    Options o;
+    Plan pl;
+  };
+  std::vector<Cand> cands{{base, pl0}};
+  if (pl0.info.path == GEMM_PATH_TCGEN05) {
+    for (int pair : {1, 2})
+      for (int bn : {128, 256})
+        for (int sk : {1, 2})
+          for (int kps : {1, 2})
+            for (int gm : {4, 8, 16}) {
+              Options o = base;
+              o.cta_pair = pair, o.block_n = bn, o.stream_k = sk, o.stage_k = kps, o.group_m = gm;
+              Plan pl;
+              if (make_plan(P, o, h->sm_count, &pl) != GEMM_OK) continue;
+              const gemm_tune_result_t c = choice_of(o, pl);
+              bool dup = false;
+              for (const Cand &x : cands) {
+                const gemm_tune_result_t d = choice_of(x.o, x.pl);
+                // two plans differ if their tiles, stage width, raster group or split differ
+                dup |= d.cta_pair == c.cta_pair && d.block_n == c.block_n &&
+                       d.stage_k == c.stage_k && d.group_m == c.group_m &&
+                       (x.pl.info.split_tiles > 0) == (pl.info.split_tiles > 0);
+              }
+              if (!dup) cands.push_back({o, pl});
+            }
+  }
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  float best = 0.0f, first = 0.0f;
+  size_t best_i = 0;
+  for (size_t i = 0; i < cands.size() && st == GEMM_OK; ++i) {
+    st = execute(h, P, cands[i].pl, s);  // warm-up: workspaces sized, code loaded
+    for (int r = 0; r < iters && st == GEMM_OK; ++r) {
+      if (r == 0 && cudaEventRecord(e0, s) != cudaSuccess) st = GEMM_ERR_CUDA;
+      if (st == GEMM_OK) st = execute(h, P, cands[i].pl, s);
+    }
+    float ms = 0.0f;
+    if (st == GEMM_OK && (cudaEventRecord(e1, s) != cudaSuccess ||
+                          cudaEventSynchronize(e1) != cudaSuccess ||
+                          cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+      st = GEMM_ERR_CUDA;
+    const float us = ms * 1000.0f / static_cast<float>(iters);
+    if (i == 0) first = us;
+    if (st == GEMM_OK && (i == 0 || us < best)) best = us, best_i = i;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != GEMM_OK) {
+    cudaGetLastError();
+    return st;
+  }
+  gemm_tune_result_t r = choice_of(cands[best_i].o, cands[best_i].pl);
+  r.candidates = static_cast<int32_t>(cands.size());
+  r.best_us = best;
+  r.default_us = first;
+  TuneEntry t{M, N, K, in_dtype, out_dtype, precision_mode, a_layout, b_layout, r};
+  bool replaced = false;
+  for (TuneEntry &x : h->tuned)
+    if (x.M == M && x.N == N && x.K == K && x.in_dtype == in_dtype && x.out_dtype == out_dtype &&
+        x.precision == precision_mode && x.a_layout == a_layout && x.b_layout == b_layout)
+      x = t, replaced = true;
+  if (!replaced) h->tuned.push_back(t);
+  if (result) *result = r;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_tune_clear(gemm_handle_t h) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  h->tuned.clear();
+  return GEMM_OK;
 }
 
 GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
@@ -1071,7 +1229,7 @@ GEMM_API gemm_status_t gemm_plan_strided(gemm_handle_t h, int64_t M, int64_t N, 
                                        precision_mode, kPlanBase, &S);
   if (st != GEMM_OK) return st;
   Plan pl;
-  st = make_plan(S.P, options_of(h), sm_count, &pl);
+  st = make_plan(S.P, options_for(h, S.P), sm_count, &pl);
   if (st != GEMM_OK) return st;
   if (info) *info = pl.info;
   if (sinfo) {
@@ -1096,7 +1254,7 @@ GEMM_API gemm_status_t gemm_run_strided(gemm_handle_t h, int64_t M, int64_t N, i
                                        precision_mode, kPlanBase, &S);
   if (st != GEMM_OK) return st;
   Plan pl;
-  st = make_plan(S.P, options_of(h), h->sm_count, &pl);  // argument checks before any work
+  st = make_plan(S.P, options_for(h, S.P), h->sm_count, &pl);  // argument checks before any work
   if (st != GEMM_OK || pl.info.path == GEMM_PATH_NONE) return st;
   DeviceGuard g(h->device);
   if (!g.ok) return GEMM_ERR_CUDA;
@@ -1115,7 +1273,7 @@ GEMM_API gemm_status_t gemm_run_strided(gemm_handle_t h, int64_t M, int64_t N, i
   st = make_strided_plan(M, N, K, A, stride_am, stride_ak, B, stride_bk, stride_bn, C, stride_cm,
                          stride_cn, in_dtype, out_dtype, precision_mode,
                          static_cast<char *>(h->st_buf), &S);
-  if (st == GEMM_OK) st = make_plan(S.P, options_of(h), h->sm_count, &pl);
+  if (st == GEMM_OK) st = make_plan(S.P, options_for(h, S.P), h->sm_count, &pl);
   if (st != GEMM_OK) return st;
   const int es = esize_of(in_dtype), os = esize_of(out_dtype);
   cudaError_t e;
@@ -1241,7 +1399,7 @@ GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int6
     const Problem P{rows, cols, K, a_blk, lda_d, b_blk, ldb_d, c_blk, ldc_d,
                     in_dtype, out_dtype, precision_mode, a_layout, b_layout};
     Plan pl;
-    st = make_plan(P, options_of(h), h->sm_count, &pl);
+    st = make_plan(P, options_for(h, P), h->sm_count, &pl);
     if (st != GEMM_OK) return st;
     st = execute(h, P, pl, s_mm);
     if (st != GEMM_OK) return st;

@@ -238,6 +238,42 @@ GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t 
                                  gemm_layout_t a_layout, gemm_layout_t b_layout,
                                  int32_t sm_count, gemm_plan_info_t *info);
 
+/* ------------------------------------------------------------------- tuning */
+
+typedef struct {
+  int32_t cta_pair;   /* GEMM_OPT_CTA_PAIR value of the choice (1 single-CTA, 2 pairs) */
+  int32_t block_n;    /* GEMM_OPT_BLOCK_N value (128 or 256) */
+  int32_t stream_k;   /* GEMM_OPT_STREAM_K value (0 auto, 1 never, 2 when possible) */
+  int32_t stage_k;    /* GEMM_OPT_STAGE_K value (1 or 2) */
+  int32_t group_m;    /* GEMM_OPT_GROUP_M value */
+  int32_t candidates; /* configurations timed */
+  float best_us;      /* mean time per product of the choice, microseconds */
+  float default_us;   /* the same for the untuned plan (the first candidate) */
+} gemm_tune_result_t;
+
+/* Times the tensor-core configurations this problem admits -- tile shape (single-CTA or
+ * CTA-pair rows, 128 or 256 columns), split-K of the last rounds, one or two K-blocks per
+ * pipeline stage, raster group height -- `iters` runs each after one warm-up, on
+ * `cuda_stream`, and keeps the fastest for the problem's signature (M, N, K, dtypes,
+ * precision, layouts): later calls on this handle with that signature (gemm_run,
+ * gemm_run_ex, gemm_plan, and the products inside gemm_run_strided and gemm_run_host)
+ * use it in place of the handle's own values of those five options. The untuned plan is
+ * one of the candidates, so the choice is never slower as measured. Blocking: returns
+ * after the last timing. It runs the real product, so C is written (with the product).
+ * Problems that do not take the plain tensor-core path (exact fp32, the fp16 accumulator,
+ * tiny or K = 0 problems) have a single candidate. `iters` in [1, 1000]. Different
+ * choices sum in different orders: results stay within the precision bounds but may
+ * differ in the last bits from the untuned plan. `result` may be NULL. */
+GEMM_API gemm_status_t gemm_tune(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+                                 int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
+                                 gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,
+                                 gemm_precision_t precision_mode, gemm_layout_t a_layout,
+                                 gemm_layout_t b_layout, void *cuda_stream, int32_t iters,
+                                 gemm_tune_result_t *result);
+
+/* Forgets every choice gemm_tune made on this handle. */
+GEMM_API gemm_status_t gemm_tune_clear(gemm_handle_t h);
+
 /* ------------------------------------------------------- six-stride interface */
 
 /* C = A @ B for any 2D views: element (i, k) of A is at A + i * stride_am + k * stride_ak,

@@ -55,6 +55,9 @@ def test_null_handle_is_rejected(L):
     assert L.gemm_run(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0) == 1
     assert L.gemm_get_status(None, None) == 1
     assert L.gemm_run_host(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0, 0, 0, None) == 1
+    assert L.gemm_tune(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0, 0, 0, None, 1,
+                       None) == 1
+    assert L.gemm_tune_clear(None) == 1
     assert L.gemm_set_option(None, 0, 1) == 1
     L.gemm_destroy(None)  # no-op
 
@@ -92,6 +95,10 @@ def test_plan_bf16_square_is_tcgen05_k_major():
     assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 128, 64, 1)
     # bandwidth-bound (125 flops per byte): two 128-byte K-blocks per stage, half the stages
     assert (p["tile_k"], p["k_iters"], p["stages"]) == (128, 64, 4)
+    # A compute-bound problem whose single-CTA tiles all fit one round keeps single CTAs.
+    p = g.plan(t((2048, 2048), torch.bfloat16), t((2048, 2048), torch.bfloat16, "col"),
+               sm_count=148)
+    assert p["cta_pair"] == 0 and (p["tile_m"], p["tile_n"], p["ctas"]) == (128, 256, 128)
     # One 128-row tile of M: single-CTA tiles.
     p = g.plan(t((128, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
                sm_count=148)
