@@ -46,6 +46,8 @@ def lib():
         L.oracle_gemm_f16acc.argtypes = [i64, i64, i64, vp, i64, i32, i32, vp, i64, i32, i32,
                                          i64, dp, i64]
         L.oracle_gemm_f16acc.restype = i32
+        L.oracle_softmax_rows.argtypes = [i64, i64, vp, i64, i32, dp, i64]
+        L.oracle_softmax_rows.restype = i32
         L.oracle_round.argtypes = [dp, i64, i32]
         L.oracle_round.restype = i32
         L.oracle_decode.argtypes = [i32, ctypes.c_uint64]
@@ -143,6 +145,18 @@ def gemm_f16acc(a, b, M, N, K, *, lda, ldb, a_dtype, b_dtype, BK, a_layout="row"
                                   C.ctypes.data, max(N, 1))
     _check(rc)
     return C
+
+
+def softmax_rows(x, M, N, *, ldx, x_dtype):
+    """Row softmax of the M x N row-major matrix in ``x`` (raw storage, leading dimension
+    ``ldx``), in fp64: y = exp(x - max) / sum(exp(x - max)) per row."""
+    x = np.ascontiguousarray(x, dtype=_STORAGE[x_dtype]).reshape(-1)
+    if M > 0 and N > 0 and x.size < (M - 1) * ldx + N:
+        raise ValueError("x is smaller than its logical extent")
+    Y = np.zeros((M, N), dtype=np.float64)
+    _check(lib().oracle_softmax_rows(M, N, x.ctypes.data, ldx, DTYPES[x_dtype], Y.ctypes.data,
+                                     max(N, 1)))
+    return Y
 
 
 def round_to(x, dtype):

@@ -33,6 +33,12 @@
  *                           then added into an fp16 running total);
  *   oracle_round         -- round-to-nearest-even into fp16 / bf16 / fp32.
  *
+ * And the second workload the pages point to, the row softmax of "Triton from
+ * zero, Lesson 4: Block Pointers", homework 4 (the masked columns of a tile are
+ * set to -inf before the max, so they add exp(-inf) = 0 to the sum):
+ *   oracle_softmax_rows  -- y[i,j] = exp(x[i,j] - m_i) / sum_k exp(x[i,k] - m_i),
+ *                           m_i = max_k x[i,k], in fp64 over the row's N values.
+ *
  * Build: gcc -O3 -fopenmp -ffp-contract=off -shared -fPIC (oracle/build.py).
  * -ffp-contract=off keeps a*b+c as two roundings on every host, so x86_64 and
  * aarch64 builds give bit-identical results.
@@ -364,5 +370,40 @@ int oracle_gemm_f16acc(int64_t M, int64_t N, int64_t K,
       }
       C[i * ldc + j] = acc;
     }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------ row softmax */
+
+/* Row softmax of an M x N row-major matrix X (leading dimension ldx, any stored
+ * format), written as fp64 to Y (leading dimension ldy). Per row, in the order of
+ * the homework's kernel: the maximum m over the row's N values, then
+ * p_j = exp(x_j - m), their sum l, and y_j = p_j / l. Only the N logical values
+ * of a row take part: the kernel's -inf padding of the tile's extra columns adds
+ * nothing to the max or the sum. IEEE rules apply throughout: a row holding a NaN
+ * or +inf, or only -inf values, gives NaN (m - m or x - m is NaN). */
+int oracle_softmax_rows(int64_t M, int64_t N, const void *X, int64_t ldx, int x_dtype,
+                        double *Y, int64_t ldy) {
+  if (M < 0 || N < 0 || x_dtype < OR_F32 || x_dtype > OR_F64) return OR_EINVAL;
+  if (ldx < (N > 0 ? N : 1) || ldy < (N > 0 ? N : 1)) return OR_EINVAL;
+  if (N == 0) return OR_OK;
+  double *p = (double *)malloc((size_t)N * sizeof(double));
+  if (!p) return OR_ENOMEM;
+  for (int64_t i = 0; i < M; ++i) {
+    double m = -INFINITY;
+    int nan = 0;
+    for (int64_t j = 0; j < N; ++j) {
+      const double x = dec_elem(X, x_dtype, i * ldx + j);
+      if (isnan(x)) nan = 1;
+      if (x > m) m = x;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+      p[j] = exp(dec_elem(X, x_dtype, i * ldx + j) - m);
+      l += p[j];
+    }
+    for (int64_t j = 0; j < N; ++j) Y[i * ldy + j] = nan ? NAN : p[j] / l;
+  }
+  free(p);
   return OR_OK;
 }
