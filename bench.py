@@ -1,7 +1,8 @@
 """Benchmark of the GB300 blocked GEMM library; prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload bf16_8192|bf16_4096|tf32_4096|exact_4096|f16acc_4096|bf16_skinny]
+                    [--workload bf16_8192|bf16_4096|tf32_4096|exact_4096|f16acc_4096|bf16_skinny|
+                               softmax_<M>x<N>]
 
 A step is one C = A @ B over one batch of seeded synthetic inputs already resident
 in HBM. Default workload: bf16 M = N = K = 8192, A row-major, B column-major,
@@ -252,6 +253,130 @@ def run_reference(args, p, desc):
                     "d2h_bytes_per_step": 0}}
 
 
+SOFTMAX_METRIC = "row softmax HBM GB/s (M x N fp32 in and out; one read and one write)"
+
+
+def softmax_workload(name):
+    """(M, N, description) of a row-softmax workload name 'softmax_<M>x<N>'."""
+    M, N = (int(v) for v in name[len("softmax_"):].split("x"))
+    return M, N, ("row softmax of an fp32 %d x %d matrix, N(0,1)*3 entries, fp32 out "
+                  "(Lesson 4, homework 4)" % (M, N))
+
+
+def softmax_input(M, N, seed=7):
+    gen = torch.Generator().manual_seed(seed)
+    return torch.randn(M, N, generator=gen) * 3.0
+
+
+def softmax_oracle_rate(x, target_s):
+    """Oracle GB/s on whole rows, as many as fit about target_s seconds (1 thread)."""
+    import oracle
+    M, N = x.shape
+    flat = x.numpy().reshape(-1)
+    r = 1
+    while True:
+        t0 = time.perf_counter()
+        oracle.softmax_rows(flat[:r * N], r, N, ldx=N, x_dtype="f32")
+        dt = time.perf_counter() - t0
+        if dt >= target_s or r >= M:
+            return r, dt, 8.0 * r * N / dt / 1e9
+        r = min(M, max(r + 1, int(r * min(8.0, 1.5 * target_s / max(dt, 1e-4)))))
+
+
+def run_softmax(args):
+    """The row-softmax workload: one step = softmax of one M x N matrix, inputs resident,
+    rotated over buffer sets larger than L2."""
+    M, N, desc = softmax_workload(args.workload)
+    x_cpu = softmax_input(M, N)
+    byts = 8.0 * M * N  # fp32 read + fp32 write
+    if args.impl == "reference":
+        r, dt, rate = softmax_oracle_rate(x_cpu, 100.0 / max(1, args.steps + args.warmup))
+        sample = "per step %d of %d rows (N=%d), fp64 oracle, 1 thread" % (r, M, N)
+        print(json.dumps({
+            "impl": "reference", "metric": SOFTMAX_METRIC, "value": rate, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "M": M, "N": N},
+            "cpu_baseline": {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": rate, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import dense_tiled_gemm_05_gb300 as g
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    h = g.Gemm(0)
+    stream = torch.cuda.current_stream(dev)
+    xs = [x_cpu.to(dev) for _ in range(max(1, args.rotate))]
+    ys = [torch.empty_like(xs[0]) for _ in xs]
+    for i in range(args.warmup):
+        h.softmax_rows(xs[i % len(xs)], out=ys[i % len(xs)])
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = h.launch_count()
+    with ClockSampler(0) as clocks:
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            h.softmax_rows(xs[i % len(xs)], out=ys[i % len(xs)])
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = h.launch_count() - launches0
+    elapsed_ms = t0.elapsed_time(t1)
+    kernel_ms = statistics.fmean(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+    value = byts * args.steps / (elapsed_ms / 1e3) / 1e9
+    peaks, peak_src = measured_peaks()
+    achieved = byts / (kernel_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "peak_source": "%s hbm_gbs (copy)" % peak_src}
+    e2e = None
+    if not args.no_e2e:  # pinned host matrix in, softmax, result back, every step
+        hx = x_cpu.pin_memory()
+        hy = torch.empty_like(hx).pin_memory()
+        dx, dy = xs[0], ys[0]
+        for _ in range(3):
+            dx.copy_(hx, non_blocking=True)
+            h.softmax_rows(dx, out=dy)
+            hy.copy_(dy, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            dx.copy_(hx, non_blocking=True)
+            h.softmax_rows(dx, out=dy)
+            hy.copy_(dy, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1)
+        e2e = {"value": byts * args.e2e_steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hx.numel() * 4, "d2h_bytes_per_step": hy.numel() * 4,
+               "ms_per_step": e_ms / args.e2e_steps}
+    if h.status() != 0:
+        raise SystemExit("device status error")
+    line = {
+        "metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": desc, "M": M, "N": N,
+                   "l2": "inputs larger than L2, rotated over %d buffer sets" % len(xs),
+                   "parallelism": "single GPU"},
+        "roofline": roof, "clocks": clocks.summary(), "e2e": e2e, "gpu_launches": launches,
+    }
+    if not args.no_cpu_baseline:
+        r, dt, rate = softmax_oracle_rate(x_cpu, 10.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": "%d of %d rows (N=%d) in fp64, %.1f s, 1 thread"
+                                          % (r, M, N, dt)}
+    print(json.dumps(line), flush=True)
+    h.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -270,6 +395,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload.startswith("softmax_"):
+        if world > 1:
+            raise SystemExit("the softmax workload runs on one GPU")
+        run_softmax(args)
+        return
     p, desc, bound = workload(args.workload)
 
     if args.impl == "reference":

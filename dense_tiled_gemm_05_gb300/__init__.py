@@ -43,7 +43,8 @@ _TORCH_OF = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_status",
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
            "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments", "gemm_run_host",
-           "gemm_run_strided", "gemm_plan_strided", "gemm_tune", "gemm_tune_clear")
+           "gemm_run_strided", "gemm_plan_strided", "gemm_tune", "gemm_tune_clear",
+           "gemm_softmax_rows")
 
 
 class GemmError(RuntimeError):
@@ -123,6 +124,8 @@ def lib():
                 L.gemm_plan_strided.restype = i32
                 L.gemm_tune.argtypes = run_args + [i32, i32, vp, i32, ctypes.POINTER(TuneResult)]
                 L.gemm_tune.restype = i32
+                L.gemm_softmax_rows.argtypes = [vp, i64, i64, vp, i64, vp, i64, i32, i32, vp]
+                L.gemm_softmax_rows.restype = i32
                 L.gemm_tune_clear.argtypes = [vp]
                 L.gemm_tune_clear.restype = i32
                 L.gemm_get_status.argtypes = [vp, vp]
@@ -289,6 +292,30 @@ class Gemm:
         _check(code, "gemm_tune")
         return r.as_dict()
 
+    def softmax_rows(self, x, out=None, out_dtype=None, stream=None):
+        """Row softmax of a CUDA matrix with unit column stride (Lesson 4, homework 4):
+        out[i] = exp(x[i] - max(x[i])) / sum(exp(x[i] - max(x[i]))). ``out=x`` runs in
+        place."""
+        if not x.is_cuda or x.dim() != 2:
+            raise ValueError("x must be a 2-D CUDA tensor")
+        M, N = x.shape
+        if N > 1 and x.stride(1) != 1:
+            raise ValueError("rows of x must be contiguous")
+        if out is None:
+            od = _TORCH_OF[_dtype_code(out_dtype)] if out_dtype is not None else x.dtype
+            out = torch.empty((M, N), dtype=od, device=x.device)
+        if out.shape != (M, N) or (N > 1 and out.stride(1) != 1):
+            raise ValueError("out must be an M x N tensor with contiguous rows")
+        s = torch.cuda.current_stream(x.device) if stream is None else stream
+        code = lib().gemm_softmax_rows(self._h, M, N, ctypes.c_void_p(x.data_ptr()),
+                                       max(x.stride(0) if M > 1 else N, N, 1),
+                                       ctypes.c_void_p(out.data_ptr()),
+                                       max(out.stride(0) if M > 1 else N, N, 1),
+                                       _dtype_code(x.dtype), _dtype_code(out.dtype),
+                                       ctypes.c_void_p(s.cuda_stream))
+        _check(code, "gemm_softmax_rows")
+        return out
+
     def tune_clear(self):
         _check(lib().gemm_tune_clear(self._h), "gemm_tune_clear")
 
@@ -395,6 +422,11 @@ def handle(device=None):
 def matmul(a, b, out=None, out_dtype=None, precision="default"):
     """C = a @ b with the default handle of a's device; see :meth:`Gemm.matmul`."""
     return handle(a.device.index).matmul(a, b, out=out, out_dtype=out_dtype, precision=precision)
+
+
+def softmax_rows(x, out=None, out_dtype=None):
+    """Row softmax with the default handle of x's device; see :meth:`Gemm.softmax_rows`."""
+    return handle(x.device.index).softmax_rows(x, out=out, out_dtype=out_dtype)
 
 
 def matmul_host(a, b, out=None, out_dtype=None, precision="default", device=None):

@@ -1019,6 +1019,35 @@ GEMM_API gemm_status_t gemm_tune_clear(gemm_handle_t h) {
   return GEMM_OK;
 }
 
+// ------------------------------------------------------------------ row softmax
+
+GEMM_API gemm_status_t gemm_softmax_rows(gemm_handle_t h, int64_t M, int64_t N, const void *X,
+                                         int64_t ldx, void *Y, int64_t ldy, gemm_dtype_t in_dtype,
+                                         gemm_dtype_t out_dtype, void *cuda_stream) {
+  if (!h || M < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!X || !Y || ldx < N || ldy < N) return GEMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  const int ies = esize_of(in_dtype), oes = esize_of(out_dtype);
+  if (reinterpret_cast<uintptr_t>(X) % ies || reinterpret_cast<uintptr_t>(Y) % oes)
+    return GEMM_ERR_ALIGNMENT;
+  // In place is allowed (the homework's kernel overwrites its input); any other overlap
+  // is not.
+  const bool in_place = X == Y && ldx == ldy && in_dtype == out_dtype;
+  uintptr_t xl, xh, yl, yh;
+  span_of(X, M, N, ldx, GEMM_ROW_MAJOR, ies, &xl, &xh);
+  span_of(Y, M, N, ldy, GEMM_ROW_MAJOR, oes, &yl, &yh);
+  if (!in_place && xl < yh && yl < xh) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  const cudaError_t e = softmax_rows_launch(X, ldx, in_dtype, Y, ldy, out_dtype, M, N, h->sm_count,
+                                            static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "softmax launch");
+  h->launches += 1;
+  return GEMM_OK;
+}
+
 GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
                                 int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
                                 gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,

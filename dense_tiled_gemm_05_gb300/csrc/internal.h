@@ -114,6 +114,12 @@ cudaError_t split3_launch(const float *src, int64_t lds, bool k_contig, float *d
 cudaError_t strided_copy_launch(const void *src, int64_t s0, int64_t s1, void *dst, int64_t d0,
                                 int64_t d1, int64_t n0, int64_t n1, int esize, cudaStream_t s);
 
+// Row softmax y = exp(x - max) / sum(exp(x - max)) of an M x N row-major matrix (fp32
+// arithmetic; any of the three dtypes in and out; X == Y with equal ld and dtype allowed).
+cudaError_t softmax_rows_launch(const void *X, int64_t ldx, int in_dtype, void *Y, int64_t ldy,
+                                int out_dtype, int64_t M, int64_t N, int sm_count,
+                                cudaStream_t s);
+
 // C[i, j] = 0 for i < M, j < N.
 cudaError_t zero_fill_launch(void *C, int64_t ldc, int64_t M, int64_t N, int out_dtype,
                              cudaStream_t s);

@@ -238,6 +238,22 @@ GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t 
                                  gemm_layout_t a_layout, gemm_layout_t b_layout,
                                  int32_t sm_count, gemm_plan_info_t *info);
 
+/* ------------------------------------------------------------- row softmax */
+
+/* Row softmax, the second workload of the pages ("Triton from zero, Lesson 4: Block
+ * Pointers", homework 4): for each of the M rows of the row-major matrix X (leading
+ * dimension ldx >= N, in elements),
+ *     Y[i, j] = exp(X[i, j] - m_i) / sum_k exp(X[i, k] - m_i),   m_i = max_k X[i, k],
+ * over the row's N values only (the homework's -inf padding of a tile's extra columns adds
+ * nothing). Y is row-major with ldy >= N; bytes of Y past column N are untouched. In
+ * place (Y == X, ldy == ldx, same dtype) is allowed; other overlaps are
+ * GEMM_ERR_INVALID_ARG. Arithmetic in fp32; in_dtype and out_dtype any of the three. A row
+ * holding a NaN or +inf, or only -inf, gives NaN (as the formula does). M == 0 or N == 0
+ * is a no-op. Asynchronous on `cuda_stream`. */
+GEMM_API gemm_status_t gemm_softmax_rows(gemm_handle_t h, int64_t M, int64_t N, const void *X,
+                                         int64_t ldx, void *Y, int64_t ldy, gemm_dtype_t in_dtype,
+                                         gemm_dtype_t out_dtype, void *cuda_stream);
+
 /* ------------------------------------------------------------------- tuning */
 
 typedef struct {
