@@ -435,7 +435,8 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
     // With a split-K share every cluster takes part, even when there are fewer tiles.
     int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
     if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
-    const bool split = !chunked && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
+    // (the fp16 accumulator never splits: its running total takes the chunks in order)
+    const bool split = !pl.variant.f16acc && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
                        sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(I.k_iters),
                                    static_cast<int32_t>(clusters), true) < tiles;
     I.ctas = 2 * (split || tiles > clusters ? clusters : tiles);
@@ -446,7 +447,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   }
   I.workspace_bytes = static_cast<int64_t>(cursor);
   I.cta_pair = pl.variant.pair ? 1 : 0;
-  if (pl.variant.pair && !chunked) {
+  if (pl.variant.pair && !pl.variant.f16acc) {
     const int32_t slots = static_cast<int32_t>(I.ctas / 2);
     const int32_t t = static_cast<int32_t>(tiles);
     if (use_split_k(opt.stream_k, t, I.k_iters, slots))
@@ -650,12 +651,13 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   // Split-K share of the last rounds (CTA-pair kernel): whole tiles otherwise.
   const int32_t tiles = tp.tiles_m * tp.tiles_n;
   tp.sk_dp_tiles = tiles;
-  if (pl.variant.pair && !pl.variant.exact && !pl.variant.f16acc && sk.h) {
+  if (pl.variant.pair && !pl.variant.f16acc && sk.h) {
     const int32_t slots = static_cast<int32_t>(grid / 2);
     tp.sk_dp_tiles = sk_dp_tiles(tiles, tp.k_blocks, slots,
                                  use_split_k(sk.mode, tiles, tp.k_blocks, slots));
     if (tp.sk_dp_tiles < tiles) {
-      const size_t flag_bytes = static_cast<size_t>(slots) * 2 * 4 * sizeof(int);
+      // one flag per epilogue warp of each CTA (4 in the CTA-pair kernel, 8 in the chunked one)
+      const size_t flag_bytes = static_cast<size_t>(slots) * 2 * 8 * sizeof(int);
       const size_t flag_region = (flag_bytes + 255) / 256 * 256;
       const size_t part_bytes =
           static_cast<size_t>(slots) * 2 * kTcBlockM * pl.variant.block_n * sizeof(float);

@@ -33,7 +33,7 @@ struct TcParams {
   // split-K share of the last rounds (CTA-pair kernel; see sk_schedule.h)
   int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
   float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32
-  int *sk_flags;          // [worker][cta rank][4 epilogue warps]
+  int *sk_flags;          // [worker][cta rank][8]: one flag per epilogue warp (4 or 8 used)
   int32_t sk_epoch;       // value this launch's writers store in their flags
 };
 
@@ -63,8 +63,10 @@ cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtenso
 int tc2_max_active_clusters();
 // Chunked kernel (CTA pairs, 256 x 256 tiles, K-major operands, register accumulators):
 // exact fp32 on split tf32 operands, or (f16acc) fp16 inputs with an fp16 accumulator.
+// tmP: split-K partial tiles (exact mode), as for the CTA-pair kernel.
 cudaError_t tc_chunk_launch(bool f16acc, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                            const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s);
+                            const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p,
+                            int grid, cudaStream_t s);
 int tc_chunk_max_active_clusters(bool f16acc);
 // K-blocks of 32 split products the exact kernel accumulates in TMEM before adding the
 // partial into its fp32 register sums. The tensor cores' accumulation keeps fewer bits

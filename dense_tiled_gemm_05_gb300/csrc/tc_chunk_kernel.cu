@@ -22,6 +22,13 @@
 //   with an fp16 add (round to nearest even). One chunk is a multiple of the 16-long K of
 //   one tcgen05.mma.kind::f16.
 //
+// In exact mode the last, partly filled rounds of tiles may be split along K over all
+// clusters (the schedule of sk_schedule.h, as in the CTA-pair kernel): a piece without its
+// tile's last K-block stores its fp32 register sums to the handle's workspace and raises a
+// flag; the piece holding the last K-block adds the lower-numbered workers' partials into
+// its register sums in increasing worker order before storing. The fp16 accumulator never
+// splits: its running total must see the chunks one after another.
+//
 // Roles (320 threads per CTA, clusters of two CTAs, 256 x 256 tile per cluster):
 //   warp 0      TMA producer (both CTAs): 128 rows of A, 128 columns of B per 128-byte K-block;
 //   warp 1      MMA issuer (leader CTA): tcgen05.mma.cta_group::2, M=256, N=256;
@@ -137,7 +144,8 @@ __device__ __forceinline__ void store_regs(const float (&v)[kXCols], const CUten
 template <bool F16ACC>
 __global__ void __launch_bounds__(kXThreads, 1)
     tc_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                    const TcParams p) {
   using G = CfgX<F16ACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -181,21 +189,32 @@ __global__ void __launch_bounds__(kXThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
-  const int num_tiles = p.tiles_m * p.tiles_n;
   const int cluster_id = blockIdx.x / 2;
   const int num_clusters = gridDim.x / 2;
+  // Whole tiles round-robin over the clusters, then (exact mode) the split-K share.
+  const SkSchedule sched = sk_make(p.tiles_m * p.tiles_n, p.k_blocks, num_clusters, p.sk_dp_tiles);
+  // Chunks are whole K-blocks in exact mode (the issuer then decides once per K-block);
+  // the fp16 accumulator may round every one or few MMAs.
+  const bool by_block = chunk % G::K_STEPS == 0;
+  const int chunk_kb = by_block ? chunk / G::K_STEPS : 1;
+  auto chunks_of = [&](const SkSegment &seg) {
+    const int len = seg.kb_end - seg.kb_begin;
+    return by_block ? (len + chunk_kb - 1) / chunk_kb : (len * G::K_STEPS + chunk - 1) / chunk;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
-      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      WorkIter work(sched, cluster_id);
+      SkSegment seg;
+      while (ok && work.next(seg)) {
         int pm, pn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+        tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
         const int m0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM;
         const int n0 = pn * G::BN + static_cast<int>(rank) * G::BN_HALF;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
@@ -221,9 +240,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
       // Four MMAs per K-block. When chunks are whole K-blocks (always in exact mode) the
       // chunk decisions are taken once per K-block and the four MMAs issue back to back:
       // this single thread's issue rate bounds the kernel, and per-MMA branching was
-      // measured to cost up to half of the throughput.
-      const bool by_block = chunk % G::K_STEPS == 0;
-      const int chunk_kb = by_block ? chunk / G::K_STEPS : 1;
+      // measured to cost up to half of the throughput. Chunks start at each piece's first
+      // K-block.
       auto take_acc = [&](uint32_t &d_tmem) {  // a fresh accumulator for the next chunk
         if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, wd)) return false;
         tc_fence_after();
@@ -235,11 +253,13 @@ __global__ void __launch_bounds__(kXThreads, 1)
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       };
-      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      WorkIter work(sched, cluster_id);
+      SkSegment seg;
+      while (ok && work.next(seg)) {
         uint32_t d_tmem = 0;
         int left = 0;  // per-MMA chunks: MMAs left in the current chunk (0: start one)
-        for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
-          const int in_chunk = by_block ? kb % chunk_kb : 0;
+        for (int kb = seg.kb_begin; ok && kb < seg.kb_end; ++kb) {
+          const int in_chunk = by_block ? (kb - seg.kb_begin) % chunk_kb : 0;
           if (by_block && in_chunk == 0 && !take_acc(d_tmem)) {
             ok = false;
             break;
@@ -251,7 +271,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t b_base = a_base + G::A_BYTES;
-          const bool last_kb = kb == p.k_blocks - 1;
+          const bool last_kb = kb == seg.kb_end - 1;
           if (by_block) {
 #pragma unroll
             for (int kk = 0; kk < G::K_STEPS; ++kk) {
@@ -305,9 +325,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const int half = e >> 2;  // which 128 columns of the tile
     uint8_t *sb = smem + G::EPI_OFFSET + e * kStoreBufBytes;
     uint32_t acc = 0, acc_phase = 0;
-    const int chunks = (p.k_blocks * G::K_STEPS + chunk - 1) / chunk;
     bool ok = true;
-    for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+    WorkIter work(sched, cluster_id);
+    SkSegment seg;
+    while (ok && work.next(seg)) {
+      const int chunks = chunks_of(seg);
       // The tile's running sums start at zero once: fp32 values (exact mode) or fp16 pairs
       // (fp16 accumulator; +0 is the all-zero bit pattern).
       float sum[F16ACC ? 1 : G::COLS];
@@ -353,8 +375,43 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (acc == 0) acc_phase ^= 1;
       }
       if (!ok) break;
+      // Split-K pieces (exact mode only): this warp's 32 x 128 block of the tile lives at
+      // rows (worker * 2 + rank) * 128 + quarter * 32 of the workspace, columns half * 128.
+      const int part_row = quarter * 32;
+      int *const flags = p.sk_flags;
+      if constexpr (!F16ACC) {
+      if (seg.role == kSegPartial) {
+        store_regs_tma<GEMM_F32>(sum, &tmP, sb, lane, (cluster_id * 2 + rank) * G::BM + part_row,
+                                 half * G::COLS, INT32_MAX, G::BN);
+        if (lane == 0) {
+          bulk_wait_group<0>();  // the partial's writes are complete
+          fence_proxy_async_global();
+          st_release_gpu(flags + (cluster_id * 2 + rank) * kXEpiWarps + e, p.sk_epoch);
+        }
+        __syncwarp();
+        goto next_segment;
+      }
+      if (seg.role == kSegOwner) {
+        // add the partials of the workers that computed the start of this tile, lowest first
+        for (int w = seg.first_src; ok && w <= seg.last_src; ++w) {
+          ok = wait_flag(flags + (w * 2 + rank) * kXEpiWarps + e, p.sk_epoch, wd);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const float4 *src = reinterpret_cast<const float4 *>(
+              p.sk_partials + (static_cast<int64_t>((w * 2 + rank) * G::BM + part_row + lane)) *
+                                  G::BN + half * G::COLS);
+#pragma unroll
+          for (int j = 0; j < G::COLS / 4; ++j) {
+            const float4 v = src[j];
+            sum[4 * j] += v.x, sum[4 * j + 1] += v.y, sum[4 * j + 2] += v.z, sum[4 * j + 3] += v.w;
+          }
+        }
+        if (!ok) break;
+      }
+      }
+      {
       int pm, pn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
+      tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
       const int row0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM + quarter * 32;
       const int col0 = pn * G::BN + half * G::COLS;
       float out[kXCols];
@@ -367,6 +424,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
         store_regs<GEMM_F16>(out, &tmC, sb, p, lane, row0, col0);
       else
         store_regs<GEMM_F32>(out, &tmC, sb, p, lane, row0, col0);
+      }
+    next_segment:;
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -429,13 +488,13 @@ int max_active_clusters() {
 
 template <bool F16ACC>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                   const TcParams &p, int grid, cudaStream_t s) {
+                   const CUtensorMap &tmP, const TcParams &p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(
       tc_chunk_kernel<F16ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgX<F16ACC>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = chunk_config<F16ACC>(grid, s, attr);
-  return cudaLaunchKernelEx(&cfg, tc_chunk_kernel<F16ACC>, tmA, tmB, tmC, p);
+  return cudaLaunchKernelEx(&cfg, tc_chunk_kernel<F16ACC>, tmA, tmB, tmC, tmP, p);
 }
 
 }  // namespace
@@ -445,8 +504,10 @@ int tc_chunk_max_active_clusters(bool f16acc) {
 }
 
 cudaError_t tc_chunk_launch(bool f16acc, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                            const CUtensorMap &tmC, const TcParams &p, int grid, cudaStream_t s) {
-  return f16acc ? launch<true>(tmA, tmB, tmC, p, grid, s) : launch<false>(tmA, tmB, tmC, p, grid, s);
+                            const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p,
+                            int grid, cudaStream_t s) {
+  return f16acc ? launch<true>(tmA, tmB, tmC, tmP, p, grid, s)
+                : launch<false>(tmA, tmB, tmC, tmP, p, grid, s);
 }
 
 }  // namespace gemm_gb300

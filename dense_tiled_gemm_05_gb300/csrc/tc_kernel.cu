@@ -273,7 +273,7 @@ int tc_stages(const TcVariant &v) {
 cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p, int grid,
                       cudaStream_t s) {
-  if (v.exact || v.f16acc) return tc_chunk_launch(v.f16acc, tmA, tmB, tmC, p, grid, s);
+  if (v.exact || v.f16acc) return tc_chunk_launch(v.f16acc, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.pair) return tc2_launch(v, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.esize == 2 && v.block_n == 256) return launch_majors<2, 256>(v, tmA, tmB, tmC, p, grid, s);
   if (v.esize == 4 && v.block_n == 256 && !v.a_mn && !v.b_mn)

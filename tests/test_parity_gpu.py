@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_util import (check_sampled, check_sums, oracle_rows, rel_err, run_gpu, to_device,
-                      tolerance)
+from gpu_util import (check_sampled, check_sums, oracle_rows, rel_err, run_gpu, sample_rows,
+                      to_device, tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -406,4 +406,30 @@ def test_wide_stages_integer_exact(block_n, stream_k):
     p = W.integer_problem(300, 200, 64, "bf16", seed=49)  # row-major B: MN-major
     with pytest.raises(g.GemmError):
         run_gpu(h2, p)
+    h2.close()
+
+
+@pytest.mark.parametrize("M,N,K,max_ctas", [(1030, 530, 1200, 0), (600, 600, 1000, 16),
+                                            (256, 256, 4096, 0), (1500, 1300, 700, 10)])
+def test_exact_split_k(M, N, K, max_ctas):
+    # Exact fp32 with the last rounds split along K: partial pieces store their fp32
+    # register sums, owners add them in worker order. Integer inputs must stay bit exact;
+    # real inputs within the exact-mode bound; two runs bitwise equal.
+    import dense_tiled_gemm_05_gb300 as g
+    h2 = g.Gemm(0)
+    h2.set_option("stream_k", 2)
+    if max_ctas:
+        h2.set_option("max_ctas", max_ctas)
+    p = W.integer_problem(M, N, K, "f32", seed=M + 3 * K)
+    plan = h2.plan(to_device(p.A), to_device(p.B), out_dtype="f32", precision="exact")
+    assert plan["path"] == "tcgen05_3xtf32" and plan["split_tiles"] > 0, plan
+    c = run_gpu(h2, p)
+    assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    q = W.ragged(M, N, K, seed=K, dtype="f32")
+    c1 = run_gpu(h2, q)
+    c2 = run_gpu(h2, q)
+    assert torch.equal(c1, c2)
+    rows = sample_rows(q.M, n_random=16)
+    C64, D = oracle_rows(q, rows)
+    assert rel_err(c1[rows], C64, D) <= tolerance(q)
     h2.close()
