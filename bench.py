@@ -48,6 +48,21 @@ CSRC = os.path.join(ROOT, "dense_tiled_gemm_05_gb300", "csrc")
 TC_SOURCES = [os.path.join(CSRC, f) for f in ("tc2_kernel.cu", "tc_common.cuh", "ptx.cuh")]
 
 
+def max_over_ranks(value, dist=None, device=None):
+    """The largest `value` over all ranks (the slowest replica's time); `value` itself on
+    one process. Replicas share nothing else: the product is not sharded."""
+    if dist is None:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, elapsed_ms):
+    """Whole-job rate: the units every rank processed, over the slowest rank's time."""
+    return units_per_rank * world / (elapsed_ms / 1e3)
+
+
 def workload(name):
     """(problem, description, bound) for a named workload."""
     if name == "bf16_8192":
@@ -466,13 +481,10 @@ def main():
         raise SystemExit("device status error in the timed region")
     elapsed_ms = t_start.elapsed_time(t_end)
     kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
 
     flops = 2.0 * p.M * p.N * p.K
-    value = world * flops * args.steps / (elapsed_ms / 1e3) / 1e12
+    value = job_rate(flops * args.steps, world, elapsed_ms) / 1e12
     peaks, peak_src = measured_peaks()
     if bound == "hbm":
         achieved = algorithmic_bytes(p) / (kernel_ms / 1e3) / 1e9
@@ -525,13 +537,10 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, dist, dev)
         if h.status() != 0:
             raise SystemExit("device status error in the e2e region")
-        e2e = {"value": world * flops * args.e2e_steps / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_rate(flops * args.e2e_steps, world, e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": ha.numel() * ha.element_size() + hb.numel() * hb.element_size(),
                "d2h_bytes_per_step": hc.numel() * hc.element_size(),
                "ms_per_step": e_ms / args.e2e_steps}
