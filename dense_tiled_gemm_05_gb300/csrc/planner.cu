@@ -1,0 +1,335 @@
+// planner.cu -- argument checks and the plan of one product: which path (tensor cores,
+// chunked tensor-core kernel, FMA tiles, zero fill), tile shape, staging of each operand,
+// split-K share, and the handle options (or gemm_tune's choice) that steer it.
+//
+// The host wrapper of "Chapter 13: The Blocked Matmul Kernel" (section 13.4,
+// 01_tiled_matmul.py) reads M, K from A and N from B, checks that the inner dimensions
+// agree, lets the caller own C, and launches a (cdiv(M, BLOCK_M), cdiv(N, BLOCK_N)) grid
+// with cdiv(K, BLOCK_K) K-iterations per tile. Here the caller states M, N, K and the
+// leading dimensions explicitly, and the planner maps the same tile grid onto a
+// persistent schedule over the SMs.
+#include <cstdint>
+
+#include "api_internal.h"
+
+using namespace gemm_gb300;
+using namespace gemm_gb300::api;
+
+namespace gemm_gb300 {
+namespace api {
+
+gemm_status_t check_args(const Problem &P) {
+  if (P.M < 0 || P.N < 0 || P.K < 0) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(P.in_dtype) || !valid_dtype(P.out_dtype)) return GEMM_ERR_INVALID_ARG;
+  if (!valid_layout(P.a_layout) || !valid_layout(P.b_layout)) return GEMM_ERR_INVALID_ARG;
+  if (P.precision < GEMM_PREC_DEFAULT || P.precision > GEMM_PREC_F16_ACC)
+    return GEMM_ERR_INVALID_ARG;
+  const bool a_used = P.M > 0 && P.K > 0 && P.N > 0;
+  const bool b_used = P.K > 0 && P.N > 0 && P.M > 0;
+  const bool c_used = P.M > 0 && P.N > 0;
+  if (c_used) {
+    if (!P.C || P.ldc < P.N) return GEMM_ERR_INVALID_ARG;
+  }
+  if (a_used) {
+    if (!P.A) return GEMM_ERR_INVALID_ARG;
+    if (P.lda < (P.a_layout == GEMM_ROW_MAJOR ? P.K : P.M)) return GEMM_ERR_INVALID_ARG;
+  }
+  if (b_used) {
+    if (!P.B) return GEMM_ERR_INVALID_ARG;
+    if (P.ldb < (P.b_layout == GEMM_ROW_MAJOR ? P.N : P.K)) return GEMM_ERR_INVALID_ARG;
+  }
+  if (P.precision == GEMM_PREC_F16_ACC) {
+    if (P.in_dtype != GEMM_F16) return GEMM_ERR_UNSUPPORTED;  // the pages' fp16 inputs only
+  } else if (P.in_dtype != GEMM_F32 && P.precision != GEMM_PREC_DEFAULT) {
+    return GEMM_ERR_UNSUPPORTED;
+  }
+  if (P.M > INT32_MAX || P.N > INT32_MAX || P.K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  const int es = esize_of(P.in_dtype), os = esize_of(P.out_dtype);
+  if ((a_used && reinterpret_cast<uintptr_t>(P.A) % es) ||
+      (b_used && reinterpret_cast<uintptr_t>(P.B) % es) ||
+      (c_used && reinterpret_cast<uintptr_t>(P.C) % os))
+    return GEMM_ERR_ALIGNMENT;
+  if (c_used) {
+    uintptr_t clo, chi;
+    span_of(P.C, P.M, P.N, P.ldc, GEMM_ROW_MAJOR, os, &clo, &chi);
+    if (a_used) {
+      uintptr_t lo, hi;
+      span_of(P.A, P.M, P.K, P.lda, P.a_layout, es, &lo, &hi);
+      if (clo < hi && lo < chi) return GEMM_ERR_INVALID_ARG;
+    }
+    if (b_used) {
+      uintptr_t lo, hi;
+      span_of(P.B, P.K, P.N, P.ldb, P.b_layout, es, &lo, &hi);
+      if (clo < hi && lo < chi) return GEMM_ERR_INVALID_ARG;
+    }
+  }
+  return GEMM_OK;
+}
+
+// TMA can read an operand in place when its base is 16-byte aligned and its leading
+// dimension is a multiple of 16 bytes (a single line needs no stride).
+static bool tma_legal(const void *p, int64_t ld, int64_t outer, int es) {
+  if (reinterpret_cast<uintptr_t>(p) % 16) return false;
+  return outer <= 1 || (ld * es) % 16 == 0;
+}
+
+static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout,
+                                bool k_is_rows_dim, int es, bool force_stage, bool split3,
+                                bool k_major_only, size_t *ws_cursor) {
+  OperandPlan o{};
+  o.ptr = p;
+  o.ld = ld;
+  o.outer = layout == GEMM_ROW_MAJOR ? rows : cols;
+  o.inner = layout == GEMM_ROW_MAJOR ? cols : rows;
+  // The operand is K-major when K is its contiguous axis.
+  const bool k_inner = k_is_rows_dim ? layout == GEMM_COL_MAJOR : layout == GEMM_ROW_MAJOR;
+  o.is_b = k_is_rows_dim;
+  o.k_contig = k_inner;
+  o.rows = k_is_rows_dim ? cols : rows;
+  o.k = k_is_rows_dim ? rows : cols;
+  o.mn_major = !k_inner;
+  o.k_outer = o.outer;
+  o.k_inner = o.inner;
+  o.split3 = split3;
+  o.transpose = !split3 && o.mn_major && (es == 4 || k_major_only);
+  o.staged = split3 || o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
+  if (o.staged) {
+    if (split3) {
+      o.k_outer = o.rows;
+      o.k_inner = 3 * o.k;
+      o.mn_major = false;
+    } else if (o.transpose) {
+      o.k_outer = o.inner;
+      o.k_inner = o.outer;
+      o.mn_major = false;
+    }
+    o.staged_ld = round_up(o.k_inner, 16 / es);
+    o.ws_offset = *ws_cursor;
+    o.ws_bytes = static_cast<size_t>(o.staged_ld * o.k_outer * es);
+    *ws_cursor = static_cast<size_t>(round_up(static_cast<int64_t>(*ws_cursor + o.ws_bytes), 256));
+  }
+  return o;
+}
+
+// Whether splitting the last rounds along K pays on GB300 (interleaved measurements of
+// bf16 products): it does when at least two whole rounds come first and every tile has a
+// long K-loop (4096^3 +5.6 %, 5120^3 +7.4 %, 8192^3 +3.6 %); it does not when every tile
+// has to be split (2048^3 -26 %) or K is short (8192 x 8192 x 2048 -1.6 %), where the
+// partial-tile traffic costs more than the idle tail it saves. stream_k: 0 by this rule,
+// 1 never, 2 whenever the schedule allows.
+bool use_split_k(int stream_k, int64_t tiles, int64_t k_blocks, int64_t slots) {
+  if (stream_k == 1) return false;
+  if (stream_k == 2) return true;
+  return slots > 0 && tiles % slots != 0 && tiles / slots >= 2 && k_blocks >= 64;
+}
+
+// Tile width by a wave-quantisation cost model: a persistent grid runs
+// ceil(tiles / slots) rounds, each as long as one tile. A 128-wide tile has half the
+// flops of a 256-wide one but, measured on GB300, takes about 0.75 of its time (every MMA
+// re-reads its 128 x 16 slice of A from shared memory, so narrow MMAs are starved of
+// shared-memory bandwidth); it wins only when it fills the machine much better, e.g.
+// when N itself is at most 128.
+static int pick_block_n(int64_t M, int64_t N, int64_t k_blocks, bool pair, int stream_k, int sm_count) {
+  const int64_t rows = pair ? 2 * kTcBlockM : kTcBlockM;
+  const int64_t slots = pair ? (sm_count > 1 ? sm_count / 2 : 1) : (sm_count > 0 ? sm_count : 1);
+  const int64_t tiles_m = (M + rows - 1) / rows;
+  auto cost = [&](int64_t bn, double per_column) {
+    const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+    // With a split-K share the last round is spread over every slot: fractional rounds.
+    const bool split = pair && use_split_k(stream_k, tiles, k_blocks, slots) &&
+                       sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(k_blocks),
+                                   static_cast<int32_t>(slots), true) < tiles;
+    const double rounds = split ? static_cast<double>(tiles) / static_cast<double>(slots)
+                                : static_cast<double>((tiles + slots - 1) / slots);
+    return rounds * static_cast<double>(bn) * per_column;
+  };
+  return cost(128, 1.5) < cost(256, 1.0) ? 128 : 256;
+}
+
+gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan *out) {
+  gemm_status_t st = check_args(P);
+  if (st != GEMM_OK) return st;
+  Plan pl{};
+  pl.group_m = opt.group_m;
+  pl.stream_k = opt.stream_k;
+  gemm_plan_info_t &I = pl.info;
+  if (P.M == 0 || P.N == 0) {
+    I.path = GEMM_PATH_NONE;
+    *out = pl;
+    return GEMM_OK;
+  }
+  if (P.K == 0) {
+    I.path = GEMM_PATH_ZERO_FILL;
+    I.ctas = 1;
+    *out = pl;
+    return GEMM_OK;
+  }
+  // Exact fp32 runs on the tensor cores as three tf32 products of split operands, except
+  // for tiny problems (the pages' 8 x 8 example and smaller), which take the fp32 FMA
+  // kernel with 4 x 4 x 4 tiles; GEMM_OPT_FORCE_PATH chooses either explicitly. The fp16
+  // accumulator runs on the tensor cores when its chunk is a whole number of 16-long MMAs,
+  // else (e.g. the pages' BLOCK_K = 8) on the FMA kernel, whose K-tile is 8.
+  const bool exact = P.in_dtype == GEMM_F32 && P.precision != GEMM_PREC_TF32;
+  const bool f16acc = P.precision == GEMM_PREC_F16_ACC;
+  pl.acc_chunk = f16acc ? (opt.acc_chunk > 0 ? opt.acc_chunk : kDefaultAccChunk) : 0;
+  bool use_fma = (exact && P.M * P.N <= 256) || (f16acc && pl.acc_chunk % 16 != 0);
+  if (opt.force_path == 2) use_fma = true;
+  if (opt.force_path == 1) {
+    if (f16acc && pl.acc_chunk % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    use_fma = false;
+  }
+  const bool split = exact && !use_fma;
+  if (use_fma) {
+    pl.fma_tile = (P.M * P.N <= 256 && !f16acc) ? 4 : 128;
+    int bm, bn, bk;
+    fma_tile_shape(pl.fma_tile, &bm, &bn, &bk);
+    if (pl.acc_chunk % bk) return GEMM_ERR_UNSUPPORTED;
+    I.path = GEMM_PATH_FMA;
+    I.tile_m = bm, I.tile_n = bn, I.tile_k = bk;
+    I.grid_m = (P.M + bm - 1) / bm;
+    I.grid_n = (P.N + bn - 1) / bn;
+    I.k_iters = (P.K + bk - 1) / bk;
+    if (I.grid_m > 65535 || I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    I.ctas = I.grid_m * I.grid_n;
+    *out = pl;
+    return GEMM_OK;
+  }
+  const int es = esize_of(P.in_dtype);
+  const int os = esize_of(P.out_dtype);
+  size_t cursor = 0;
+  pl.a = plan_operand(P.A, P.M, P.K, P.lda, P.a_layout, false, es, opt.force_staging != 0, split,
+                      f16acc, &cursor);
+  pl.b = plan_operand(P.B, P.K, P.N, P.ldb, P.b_layout, true, es, opt.force_staging != 0, split,
+                      f16acc, &cursor);
+  pl.variant.esize = es;
+  pl.variant.a_mn = pl.a.mn_major;
+  pl.variant.b_mn = pl.b.mn_major;
+  // Flops per byte of A, B and C: under ~256 the product is bandwidth-bound on GB300.
+  const double intensity = 2.0 * P.M * P.N * P.K /
+                           (es * (static_cast<double>(P.M) * P.K + static_cast<double>(P.K) * P.N) +
+                            static_cast<double>(os) * P.M * P.N);
+  // CTA pairs (256-row tiles on two SMs) halve the shared-memory and L2 traffic per
+  // flop; a problem no taller than one 128-row tile keeps single-CTA tiles, and so does a
+  // compute-bound one whose 128 x 256 single-CTA tiles all run at once (one round on the
+  // SMs), where the pair's cross-SM handshakes cost more than they save (bf16 2048^3:
+  // 16.6 against 18.7 us). Bandwidth-bound ones keep pairs, for their wide stages.
+  const int64_t single_tiles = ((P.M + kTcBlockM - 1) / kTcBlockM) * ((P.N + 255) / 256);
+  const bool one_round = single_tiles <= sm_count && intensity >= 256.0;
+  pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM && !one_round);
+  pl.variant.block_n =
+      opt.block_n ? opt.block_n
+                  : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
+                                 split ? 1 : opt.stream_k, sm_count);
+  if (split || f16acc) {  // the chunked kernel has one shape: CTA pairs, 256 x 256 tiles
+    pl.variant.exact = split;
+    pl.variant.f16acc = f16acc;
+    pl.variant.pair = true;
+    pl.variant.block_n = 256;
+  }
+  const bool chunked = pl.variant.exact || pl.variant.f16acc;
+  // Two 128-byte K-blocks per stage (CTA-pair kernel, K-major 16-bit operands): each row
+  // of A and B is then fetched 256 contiguous bytes at a time. By default only for
+  // bandwidth-bound products (under ~256 flops per byte of A, B and C), where it measured
+  // +1.5 % on bf16 16384 x 128 x 8192; compute-bound ones keep the deeper ring of one
+  // K-block per stage (4096^3 lost 9 % with wide stages). A forced split-K keeps narrow
+  // K-blocks, the finer unit it shares out (one 256 x 256 x 8192 tile: 128 units for 76
+  // clusters rather than 64).
+  const bool wide_ok = pl.variant.pair && !chunked && es == 2 && !pl.a.mn_major && !pl.b.mn_major;
+  if (opt.stage_k == 2 && !wide_ok) return GEMM_ERR_UNSUPPORTED;
+  pl.variant.kps =
+      opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < 256.0 && opt.stream_k != 2)
+          ? 2
+          : 1;
+  I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : f16acc ? GEMM_PATH_TCGEN05_F16ACC : GEMM_PATH_TCGEN05;
+  I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
+  I.tile_n = pl.variant.block_n;
+  I.tile_k = pl.variant.kps * 128 / es;
+  I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
+  I.grid_n = (P.N + I.tile_n - 1) / I.tile_n;
+  const int64_t k_total = split ? 3 * P.K : P.K;  // split operands concatenate 3 products
+  I.k_iters = (k_total + I.tile_k - 1) / I.tile_k;
+  if (I.grid_m * I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  // chunked kernel: four MMAs per 128-byte K-block
+  if (split)
+    pl.chunk_steps = 4 * (opt.exact_chunk > 0 ? opt.exact_chunk : exact_chunk_kblocks(I.k_iters));
+  else if (f16acc)
+    pl.chunk_steps = static_cast<int>(pl.acc_chunk / 16);
+  I.stages = tc_stages(pl.variant);
+  I.stage_a = pl.a.staged, I.stage_b = pl.b.staged;
+  I.a_mn_major = pl.a.mn_major, I.b_mn_major = pl.b.mn_major;
+  // TMA stores need a 16-byte aligned base and row pitch; they are also used only when a
+  // row of C ends on a 16-byte boundary, because a store box clipped at a right edge that
+  // falls inside a 16-byte granule was seen to write the whole granule (past column N).
+  I.tma_store = reinterpret_cast<uintptr_t>(P.C) % 16 == 0 && (P.ldc * os) % 16 == 0 &&
+                (P.N * os) % 16 == 0;
+  const int64_t tiles = I.grid_m * I.grid_n;
+  if (pl.variant.pair) {
+    // One cluster of two CTAs per tile slot; the launch clamps to the clusters that fit.
+    // With a split-K share every cluster takes part, even when there are fewer tiles.
+    int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
+    if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
+    // (the fp16 accumulator never splits: its running total takes the chunks in order)
+    const bool split = !pl.variant.f16acc && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
+                       sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(I.k_iters),
+                                   static_cast<int32_t>(clusters), true) < tiles;
+    I.ctas = 2 * (split || tiles > clusters ? clusters : tiles);
+  } else {
+    int64_t ctas = sm_count > 0 ? sm_count : 1;
+    if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
+    I.ctas = tiles < ctas ? tiles : ctas;
+  }
+  I.workspace_bytes = static_cast<int64_t>(cursor);
+  I.cta_pair = pl.variant.pair ? 1 : 0;
+  if (pl.variant.pair && !pl.variant.f16acc) {
+    const int32_t slots = static_cast<int32_t>(I.ctas / 2);
+    const int32_t t = static_cast<int32_t>(tiles);
+    if (use_split_k(opt.stream_k, t, I.k_iters, slots))
+      I.split_tiles = t - sk_dp_tiles(t, static_cast<int32_t>(I.k_iters), slots, true);
+  }
+  *out = pl;
+  return GEMM_OK;
+}
+
+Options options_of(gemm_handle_t h) {
+  Options o;
+  if (h) {
+    o.force_path = h->force_path;
+    o.group_m = h->group_m;
+    o.max_ctas = h->max_ctas;
+    o.force_staging = h->force_staging;
+    o.cta_pair = h->cta_pair;
+    o.block_n = h->block_n;
+    o.stream_k = h->stream_k;
+    o.exact_chunk = h->exact_chunk;
+    o.acc_chunk = h->acc_chunk;
+    o.stage_k = h->stage_k;
+  }
+  return o;
+}
+
+const TuneEntry *find_tuned(gemm_handle_t h, const Problem &P) {
+  if (!h) return nullptr;
+  for (const TuneEntry &t : h->tuned)
+    if (t.M == P.M && t.N == P.N && t.K == P.K && t.in_dtype == P.in_dtype &&
+        t.out_dtype == P.out_dtype && t.precision == P.precision && t.a_layout == P.a_layout &&
+        t.b_layout == P.b_layout)
+      return &t;
+  return nullptr;
+}
+
+// The handle's options, with the tile-shape options gemm_tune chose for this problem
+// signature (if it was tuned) in place of the handle's.
+Options options_for(gemm_handle_t h, const Problem &P) {
+  Options o = options_of(h);
+  if (const TuneEntry *t = find_tuned(h, P)) {
+    o.cta_pair = t->choice.cta_pair;
+    o.block_n = t->choice.block_n;
+    o.stream_k = t->choice.stream_k;
+    o.stage_k = t->choice.stage_k;
+    o.group_m = t->choice.group_m;
+  }
+  return o;
+}
+
+}  // namespace api
+}  // namespace gemm_gb300
