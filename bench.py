@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload bf16_8192|bf16_4096|tf32_4096|exact_4096|f16acc_4096|bf16_skinny|
-                               softmax_<M>x<N>]
+                               ragged_216|softmax_<M>x<N>]
 
 A step is one C = A @ B over one batch of seeded synthetic inputs already resident
 in HBM. Default workload: bf16 M = N = K = 8192, A row-major, B column-major,
@@ -392,6 +392,95 @@ def run_softmax(args):
     h.close()
 
 
+def run_ragged(args):
+    """The ragged-edge sweep (fp16 in, fp32 accumulate and out, every M, N, K in
+    {1, 17, 127, 1000, 1023, 1025}, row-major, tight leading dimensions): one step runs all
+    216 products, inputs resident on the device."""
+    combos = W.ragged_combos()
+    probs = [W.ragged(M, N, K) for (M, N, K) in combos]
+    flops = sum(2.0 * p.M * p.N * p.K for p in probs)
+    desc = ("ragged-edge sweep: fp16 A[M,K] @ B[K,N], fp32 out, all 216 combinations of "
+            "M, N, K in {1,17,127,1000,1023,1025}, U[-1,1], row-major, tight leading dims")
+    if args.impl == "reference":
+        import oracle
+        t0 = time.perf_counter()
+        done = 0.0
+        budget = 100.0 / max(1, args.steps + args.warmup)
+        for p in probs:
+            a, al, lda = W.storage_numpy(p.A)
+            b, bl, ldb = W.storage_numpy(p.B)
+            oracle.gemm_f64(a, b, p.M, p.N, p.K, lda=lda, ldb=ldb, a_dtype="f16", b_dtype="f16",
+                            a_layout=al, b_layout=bl)
+            done += 2.0 * p.M * p.N * p.K
+            if time.perf_counter() - t0 > budget:
+                break
+        dt = time.perf_counter() - t0
+        rate = done / dt / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": rate, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc},
+            "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": "%.3g of %.3g flops of the sweep"
+                                                         % (done, flops)},
+            "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import dense_tiled_gemm_05_gb300 as g
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    h = g.Gemm(0)
+    stream = torch.cuda.current_stream(dev)
+    ops = [(p.A.to(dev), p.B.to(dev), torch.empty((p.M, p.N), device=dev)) for p in probs]
+
+    def step():
+        for a, b, c in ops:
+            h.matmul(a, b, out=c)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    # The sweep is launch-bound (hundreds of small products): capture one step in a CUDA
+    # graph and replay it, so the host's per-call cost is not what is measured.
+    graph = torch.cuda.CUDAGraph()
+    launches0 = h.launch_count()
+    with torch.cuda.graph(graph):
+        step()
+    per_step = h.launch_count() - launches0
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = per_step * args.steps
+    if h.status() != 0:
+        raise SystemExit("device status error")
+    elapsed_ms = t0.elapsed_time(t1)
+    value = flops * args.steps / (elapsed_ms / 1e3) / 1e12
+    peaks, peak_src = measured_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": desc, "products_per_step": len(ops), "cuda_graph": True,
+                   "l2": "inputs of all 216 products resident (489 MB)",
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": value / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": "%s bf16_tflops (fp16 runs at the bf16 rate); most of the "
+                                    "216 products are too small to fill the GPU" % peak_src},
+        "clocks": clocks.summary(), "e2e": None, "gpu_launches": launches,
+    }
+    print(json.dumps(line), flush=True)
+    h.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,6 +499,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload == "ragged_216":
+        if world > 1:
+            raise SystemExit("the ragged sweep runs on one GPU")
+        run_ragged(args)
+        return
     if args.workload.startswith("softmax_"):
         if world > 1:
             raise SystemExit("the softmax workload runs on one GPU")

@@ -30,7 +30,7 @@ struct gemm_handle_s {
   // options
   uint64_t timeout_us = 2000000;
   int force_path = 0;
-  int group_m = 16;  // gemm_tune chose 16 on bf16 4096^3-8192^3 and tf32 4096^3 (+1-2 %)
+  int group_m = 8;  // sustained under the power cap, bf16 8192^3: 8 > 16 > 4 > 32
   int max_ctas = 0;
   int stall_producer = 0;
   int force_staging = 0;
@@ -44,7 +44,6 @@ struct gemm_handle_s {
   // split-K workspace of the CTA-pair kernel: partial tiles and flags
   void *sk_ws = nullptr;
   size_t sk_ws_bytes = 0;
-  int32_t sk_epoch = 0;
   // host-buffer pipeline (gemm_run_host): device copies of A, B, C, streams and events
   static constexpr int kMaxPanels = 48;  // per operand; steps <= 2 * kMaxPanels
   void *hp_buf = nullptr;
@@ -106,7 +105,7 @@ struct Problem {
 };
 
 struct Options {
-  int force_path = 0, group_m = 16, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
+  int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
   int stream_k = 0, exact_chunk = 0, acc_chunk = 0, stage_k = 0;
 };
 

@@ -34,7 +34,8 @@ struct TcParams {
   int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
   float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32
   int *sk_flags;          // [worker][cta rank][8]: one flag per epilogue warp (4 or 8 used)
-  int32_t sk_epoch;       // value this launch's writers store in their flags
+  int *sk_epoch_word;     // [epoch, arrivals]: writers store epoch + 1 in their flags; the
+                          // last CTA to finish advances the epoch (see tc_common.cuh)
 };
 
 // One tensor-core kernel variant: element size of A and B (2 = f16/bf16, 4 = fp32 as tf32),

@@ -117,10 +117,6 @@ cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t 
   return repack_launch(o.ptr, o.ld, dst, o.staged_ld, o.outer, o.inner, es, s);
 }
 
-// Tensor maps, kernel parameters and launch of the tensor-core kernel for operands that
-// are already TMA-legal (in place or staged).
-// Split-K context of a launch: a workspace provider (null = split-K off).
-
 static gemm_status_t ensure_sk_workspace(gemm_handle_t h, size_t bytes, size_t flag_bytes,
                                          cudaStream_t s) {
   if (bytes <= h->sk_ws_bytes) return GEMM_OK;
@@ -134,8 +130,7 @@ static gemm_status_t ensure_sk_workspace(gemm_handle_t h, size_t bytes, size_t f
     cudaGetLastError();
     return GEMM_ERR_NO_MEMORY;
   }
-  // Flags start at 0 and every launch uses a fresh non-zero epoch, so stale flags of
-  // earlier launches never match.
+  // The epoch word, the arrival count and every flag start at 0.
   if (cudaMemsetAsync(p, 0, flag_bytes, s) != cudaSuccess) {
     cudaFree(p);
     return GEMM_ERR_CUDA;
@@ -145,6 +140,8 @@ static gemm_status_t ensure_sk_workspace(gemm_handle_t h, size_t bytes, size_t f
   return GEMM_OK;
 }
 
+// Tensor maps, kernel parameters and launch of the tensor-core kernel for operands that
+// are already TMA-legal (in place or staged).
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
                         const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,
                         int group_m, int debug_flags, SplitK sk, cudaStream_t s) {
@@ -202,21 +199,23 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
     tp.sk_dp_tiles = sk_dp_tiles(tiles, tp.k_blocks, slots,
                                  use_split_k(sk.mode, tiles, tp.k_blocks, slots));
     if (tp.sk_dp_tiles < tiles) {
-      // one flag per epilogue warp of each CTA (4 in the CTA-pair kernel, 8 in the chunked one)
-      const size_t flag_bytes = static_cast<size_t>(slots) * 2 * 8 * sizeof(int);
-      const size_t flag_region = (flag_bytes + 255) / 256 * 256;
+      // Workspace: [epoch word, arrival count | one flag per epilogue warp of each CTA of
+      // the largest grid (8 per CTA) | partial tiles]. The flag region has a fixed size, so
+      // a grown workspace never finds partial data where flags are expected.
+      const int64_t ctas_max = sk.h->sm_count > grid ? sk.h->sm_count : grid;
+      const size_t flag_region =
+          static_cast<size_t>(round_up(static_cast<int64_t>((2 + 8 * ctas_max) * sizeof(int)), 256));
       const size_t part_bytes =
           static_cast<size_t>(slots) * 2 * kTcBlockM * pl.variant.block_n * sizeof(float);
       gemm_status_t st = ensure_sk_workspace(sk.h, flag_region + part_bytes, flag_region, s);
       if (st != GEMM_OK) return st;
-      tp.sk_flags = static_cast<int *>(sk.h->sk_ws);
+      tp.sk_epoch_word = static_cast<int *>(sk.h->sk_ws);
+      tp.sk_flags = tp.sk_epoch_word + 2;
       tp.sk_partials = reinterpret_cast<float *>(static_cast<char *>(sk.h->sk_ws) + flag_region);
       // partial tiles: rows [worker][cta rank][128], block_n fp32 columns; 32 x 32 boxes
       if (!encode_2d(&tmP, GEMM_F32, tp.sk_partials, pl.variant.block_n,
                      static_cast<int64_t>(slots) * 2 * kTcBlockM, pl.variant.block_n, 32, 32))
         return GEMM_ERR_CUDA;
-      sk.h->sk_epoch = sk.h->sk_epoch == INT32_MAX ? 1 : sk.h->sk_epoch + 1;
-      tp.sk_epoch = sk.h->sk_epoch;
     }
   }
   const cudaError_t e = tc_launch(pl.variant, tmA, tmB, tmC, tmP, tp, static_cast<int>(grid), s);

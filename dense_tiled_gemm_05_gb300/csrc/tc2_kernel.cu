@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_clusters = gridDim.x / 2;
   // Whole tiles round-robin over the clusters, then the split-K share of the last rounds.
   const SkSchedule sched = sk_make(p.tiles_m * p.tiles_n, p.k_blocks, num_clusters, p.sk_dp_tiles);
+  const bool split = p.sk_dp_tiles < p.tiles_m * p.tiles_n;
+  const int epoch = split ? sk_epoch_begin(p.sk_epoch_word) : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------ producer (both CTAs)
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           bulk_wait_group<0>();  // the partial's writes are complete
           fence_proxy_async_global();
-          st_release_gpu(p.sk_flags + (cluster_id * 2 + rank) * 4 + quarter, p.sk_epoch);
+          st_release_gpu(p.sk_flags + (cluster_id * 2 + rank) * 4 + quarter, epoch);
         }
         __syncwarp();
       } else {
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // stages are idle and each epilogue warp borrows a slice of them for the TMA loads.
           uint8_t *slice = smem + e * G::OWNER_SLICE;
           for (int w = seg.first_src; ok && w <= seg.last_src; ++w) {
-            ok = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, p.sk_epoch, wd);
+            ok = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, epoch, wd);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             fence_proxy_async_global();
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
   }
+  if (split && threadIdx.x == 0) sk_epoch_end(p.sk_epoch_word, epoch);
 }
 
 template <int ESIZE, bool A_MN, bool B_MN, int BN, int KPS = 1>

@@ -193,6 +193,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
   const int num_clusters = gridDim.x / 2;
   // Whole tiles round-robin over the clusters, then (exact mode) the split-K share.
   const SkSchedule sched = sk_make(p.tiles_m * p.tiles_n, p.k_blocks, num_clusters, p.sk_dp_tiles);
+  const bool split = p.sk_dp_tiles < p.tiles_m * p.tiles_n;
+  const int epoch = split ? sk_epoch_begin(p.sk_epoch_word) : 0;
   // Chunks are whole K-blocks in exact mode (the issuer then decides once per K-block);
   // the fp16 accumulator may round every one or few MMAs.
   const bool by_block = chunk % G::K_STEPS == 0;
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (lane == 0) {
           bulk_wait_group<0>();  // the partial's writes are complete
           fence_proxy_async_global();
-          st_release_gpu(flags + (cluster_id * 2 + rank) * kXEpiWarps + e, p.sk_epoch);
+          st_release_gpu(flags + (cluster_id * 2 + rank) * kXEpiWarps + e, epoch);
         }
         __syncwarp();
         goto next_segment;
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (seg.role == kSegOwner) {
         // add the partials of the workers that computed the start of this tile, lowest first
         for (int w = seg.first_src; ok && w <= seg.last_src; ++w) {
-          ok = wait_flag(flags + (w * 2 + rank) * kXEpiWarps + e, p.sk_epoch, wd);
+          ok = wait_flag(flags + (w * 2 + rank) * kXEpiWarps + e, epoch, wd);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const float4 *src = reinterpret_cast<const float4 *>(
@@ -443,6 +445,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
   }
+  if (split && threadIdx.x == 0) sk_epoch_end(p.sk_epoch_word, epoch);
 }
 
 template <bool F16ACC>

@@ -172,6 +172,23 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
   return v;
 }
 
+// Split-K epochs. A partial writer stores `epoch` in its flag; the owner waits for that
+// value. Every CTA of a launch reads the epoch word once at its start (it is stable then:
+// only the last CTA of the previous launch changed it) and uses epoch = word + 1; the last
+// CTA of the launch to finish stores that epoch into the word. Flags left by an earlier
+// launch -- also one that gave up on a bounded wait, or a replayed graph -- hold an older
+// value and never match.
+__device__ __forceinline__ int sk_epoch_begin(const int *word) {
+  return *reinterpret_cast<const volatile int *>(word) + 1;
+}
+__device__ __forceinline__ void sk_epoch_end(int *word, int epoch) {
+  __threadfence();
+  if (atomicAdd(word + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    word[1] = 0;
+    *reinterpret_cast<volatile int *>(word) = epoch;
+  }
+}
+
 // Bounded wait until *flag == value (a split-K partial of this launch is in memory).
 __device__ __forceinline__ bool wait_flag(const int *flag, int value, const Watchdog &wd) {
   if (ld_acquire_gpu(flag) == value) return true;

@@ -70,3 +70,26 @@ def test_workspace_allocation_failure_is_reported(g, monkeypatch):
     C64, D = oracle_rows(p)
     assert rel_err(c, C64, D) <= 1e-2
     h.close()
+
+
+def test_split_k_after_a_timeout(g):
+    # A split-K launch that gives up on its waits leaves flags behind; the epoch protocol
+    # must keep the next launches from mistaking them for this launch's partials.
+    p = W.integer_problem(1030, 530, 1200, "bf16", seed=7, b_layout="col")
+    a, b = to_device(p.A), to_device(p.B)
+    ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
+    h = g.Gemm(0)
+    h.set_option("stream_k", 2)
+    assert h.plan(a, b, out_dtype="f32")["split_tiles"] > 0
+    c = h.matmul(a, b, out_dtype="f32")
+    assert h.status() == 0 and torch.equal(c.cpu().to(torch.int64), ref)
+    h.set_option("wait_timeout_us", 20000)
+    h.set_option("fault_stall_producer", 1)
+    h.matmul(a, b, out_dtype="f32")
+    assert h.status() == 6
+    h.set_option("fault_stall_producer", 0)
+    for _ in range(3):
+        c = h.matmul(a, b, out_dtype="f32")
+        assert h.status() == 0
+        assert torch.equal(c.cpu().to(torch.int64), ref)
+    h.close()

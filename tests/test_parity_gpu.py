@@ -433,3 +433,27 @@ def test_exact_split_k(M, N, K, max_ctas):
     C64, D = oracle_rows(q, rows)
     assert rel_err(c1[rows], C64, D) <= tolerance(q)
     h2.close()
+
+
+def test_north_star_signature_gemm_run(h):
+    # gemm_run: the plain C signature (row-major A and B, legacy default stream), called
+    # through ctypes with raw device pointers, on the pages' 2 x 2 check, a ragged fp16
+    # problem and an fp32 exact one.
+    import ctypes
+    import dense_tiled_gemm_05_gb300 as g
+    L = g.lib()
+    for p in (W.two_by_two("f32"), W.ragged(1000, 17, 1025, seed=5), W.small_exact()):
+        a, b = to_device(p.A.contiguous()), to_device(p.B.contiguous())
+        c = torch.full((p.M, p.N + 3), float("nan"), device="cuda")
+        code = L.gemm_run(h.handle, p.M, p.N, p.K, ctypes.c_void_p(a.data_ptr()), p.K,
+                          ctypes.c_void_p(b.data_ptr()), p.N, ctypes.c_void_p(c.data_ptr()),
+                          p.N + 3, g._dtype_code(a.dtype), g._dtype_code("f32"),
+                          g.PREC[p.precision])
+        assert code == 0
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        C64, D = oracle_rows(p)
+        assert rel_err(c[:, :p.N], C64, D) <= tolerance(p)
+        assert torch.isnan(c[:, p.N:]).all()
+        if p.M == 2:  # the pages' printed single-tile result, bit for bit
+            assert torch.equal(c[:, :2].cpu(), torch.tensor([[19.0, 22.0], [43.0, 50.0]]))
