@@ -172,24 +172,37 @@ __global__ void repack_kernel(const T *__restrict__ src, int64_t ld_src, T *__re
 }
 
 // dst[x * ld_dst + o] = src[o * ld_src + x]: `outer` source lines of `inner` elements
-// become `inner` lines of `outer` elements, through 32 x 32 shared-memory tiles so both
-// the reads and the writes are coalesced.
+// become `inner` lines of `outer` elements. A CTA moves a strip of 32 source lines by 512
+// contiguous bytes through shared memory: each warp reads 128-byte pieces of one source
+// line (consecutive pieces back to back, so every DRAM page is read in long runs) and
+// writes 128-byte pieces of one destination line; the odd row pitch of the staging tile
+// keeps both directions free of bank conflicts.
 template <typename T>
-__global__ void transpose_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
-                                 int64_t ld_dst, int64_t outer, int64_t inner) {
-  __shared__ T tile[32][33];
+__global__ void __launch_bounds__(256) transpose_kernel(const T *__restrict__ src, int64_t ld_src,
+                                                        T *__restrict__ dst, int64_t ld_dst,
+                                                        int64_t outer, int64_t inner) {
+  constexpr int S = 512 / (32 * sizeof(T));  // 32-element pieces per strip line
+  __shared__ T tile[32][32 * S + 1];
+  const int tx = threadIdx.x, ty = threadIdx.y;
   for (int64_t o0 = static_cast<int64_t>(blockIdx.y) * 32; o0 < outer;
        o0 += static_cast<int64_t>(gridDim.y) * 32) {
-    for (int64_t x0 = static_cast<int64_t>(blockIdx.x) * 32; x0 < inner;
-         x0 += static_cast<int64_t>(gridDim.x) * 32) {
-      for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-        const int64_t o = o0 + j, x = x0 + threadIdx.x;
-        if (o < outer && x < inner) tile[j][threadIdx.x] = src[o * ld_src + x];
+    for (int64_t x0 = static_cast<int64_t>(blockIdx.x) * 32 * S; x0 < inner;
+         x0 += static_cast<int64_t>(gridDim.x) * 32 * S) {
+      for (int j = ty; j < 32; j += blockDim.y) {
+        const int64_t o = o0 + j;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          const int64_t x = x0 + s * 32 + tx;
+          if (o < outer && x < inner) tile[j][s * 32 + tx] = src[o * ld_src + x];
+        }
       }
       __syncthreads();
-      for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-        const int64_t x = x0 + j, o = o0 + threadIdx.x;
-        if (x < inner && o < outer) dst[x * ld_dst + o] = tile[threadIdx.x][j];
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        for (int j = ty; j < 32; j += blockDim.y) {
+          const int64_t x = x0 + s * 32 + j, o = o0 + tx;
+          if (x < inner && o < outer) dst[x * ld_dst + o] = tile[tx][s * 32 + j];
+        }
       }
       __syncthreads();
     }
@@ -243,7 +256,8 @@ cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t outer, int64_t inner, int esize, cudaStream_t s) {
   const dim3 block(32, 8);
-  const int64_t gx = (inner + 31) / 32, gy = (outer + 31) / 32;
+  const int64_t strip = 512 / esize;  // source elements per strip line
+  const int64_t gx = (inner + strip - 1) / strip, gy = (outer + 31) / 32;
   const dim3 grid(static_cast<unsigned>(gx < 4096 ? (gx < 1 ? 1 : gx) : 4096),
                   static_cast<unsigned>(gy < 4096 ? (gy < 1 ? 1 : gy) : 4096));
   if (esize == 2)
