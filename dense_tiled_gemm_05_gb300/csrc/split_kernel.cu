@@ -35,34 +35,65 @@ __device__ __forceinline__ void put3(float *dst, int64_t ldd, int64_t K, int64_t
   row[2 * K] = is_b ? hi : lo; // segment 2: A's lo against B's hi
 }
 
-// Logical operand X[r][k] (R rows, K columns of the contraction). When k_contig, X[r][k]
-// is src[r * lds + k]; otherwise src[k * lds + r] and the tile goes through shared memory
-// so that both the reads and the writes are coalesced.
-template <bool K_CONTIG>
-__global__ void split3_kernel(const float *__restrict__ src, int64_t lds, float *__restrict__ dst,
-                              int64_t ldd, int64_t R, int64_t K, bool is_b) {
-  __shared__ float tile[32][33];
-  for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32; r0 < R;
-       r0 += static_cast<int64_t>(gridDim.y) * 32) {
-    for (int64_t k0 = static_cast<int64_t>(blockIdx.x) * 32; k0 < K;
-         k0 += static_cast<int64_t>(gridDim.x) * 32) {
-      if (K_CONTIG) {
-        for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-          const int64_t r = r0 + j, k = k0 + threadIdx.x;
-          if (r < R && k < K) put3(dst, ldd, K, r, k, src[r * lds + k], is_b);
+// Logical operand X[r][k] (R rows, K columns of the contraction), stored K-contiguous:
+// X[r][k] = src[r * lds + k]. Each thread splits 4 consecutive k of one row: one 16-byte
+// load and three 16-byte stores when the row and the destination are 16-byte aligned
+// (scalar otherwise, and at the row's ragged end).
+__global__ void __launch_bounds__(256) split3_rows_kernel(const float *__restrict__ src,
+                                                          int64_t lds, float *__restrict__ dst,
+                                                          int64_t ldd, int64_t R, int64_t K,
+                                                          bool is_b, bool vec) {
+  const int64_t kc = (K + 3) / 4;  // 4-wide chunks per row
+  for (int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; id < R * kc;
+       id += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = id / kc, k = (id - r * kc) * 4;
+    if (vec && k + 4 <= K) {
+      const float4 x = *reinterpret_cast<const float4 *>(src + r * lds + k);
+      const float4 hi = make_float4(tf32_rn(x.x), tf32_rn(x.y), tf32_rn(x.z), tf32_rn(x.w));
+      const float4 lo = make_float4(tf32_rn(x.x - hi.x), tf32_rn(x.y - hi.y), tf32_rn(x.z - hi.z),
+                                    tf32_rn(x.w - hi.w));
+      float4 *row = reinterpret_cast<float4 *>(dst + r * ldd + k);
+      row[0] = hi;                             // segment 0: hi for A and for B
+      row[K / 4] = is_b ? lo : hi;             // segment 1: A's hi against B's lo
+      row[2 * (K / 4)] = is_b ? hi : lo;       // segment 2: A's lo against B's hi
+    } else {
+      for (int64_t kk = k; kk < k + 4 && kk < K; ++kk)
+        put3(dst, ldd, K, r, kk, src[r * lds + kk], is_b);
+    }
+  }
+}
+
+// The same operand stored the other way, X[r][k] = src[k * lds + r]: a CTA moves 32 lines
+// of k by 512 contiguous bytes of r through shared memory (the strip transpose of the
+// staging copy), so both the reads and the split writes are long contiguous runs.
+__global__ void __launch_bounds__(256) split3_cols_kernel(const float *__restrict__ src,
+                                                          int64_t lds, float *__restrict__ dst,
+                                                          int64_t ldd, int64_t R, int64_t K,
+                                                          bool is_b) {
+  constexpr int S = 4;  // 32-float pieces per strip line (512 bytes)
+  __shared__ float tile[32][32 * S + 1];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int64_t k0 = static_cast<int64_t>(blockIdx.y) * 32; k0 < K;
+       k0 += static_cast<int64_t>(gridDim.y) * 32) {
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32 * S; r0 < R;
+         r0 += static_cast<int64_t>(gridDim.x) * 32 * S) {
+      for (int j = ty; j < 32; j += blockDim.y) {
+        const int64_t k = k0 + j;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          const int64_t r = r0 + s * 32 + tx;
+          if (k < K && r < R) tile[j][s * 32 + tx] = src[k * lds + r];
         }
-      } else {
-        for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-          const int64_t k = k0 + j, r = r0 + threadIdx.x;
-          if (k < K && r < R) tile[j][threadIdx.x] = src[k * lds + r];
-        }
-        __syncthreads();
-        for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-          const int64_t r = r0 + j, k = k0 + threadIdx.x;
-          if (r < R && k < K) put3(dst, ldd, K, r, k, tile[threadIdx.x][j], is_b);
-        }
-        __syncthreads();
       }
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        for (int j = ty; j < 32; j += blockDim.y) {
+          const int64_t r = r0 + s * 32 + j, k = k0 + tx;
+          if (r < R && k < K) put3(dst, ldd, K, r, k, tile[tx][s * 32 + j], is_b);
+        }
+      }
+      __syncthreads();
     }
   }
 }
@@ -71,14 +102,23 @@ __global__ void split3_kernel(const float *__restrict__ src, int64_t lds, float 
 
 cudaError_t split3_launch(const float *src, int64_t lds, bool k_contig, float *dst, int64_t ldd,
                           int64_t R, int64_t K, bool is_b, cudaStream_t s) {
-  const dim3 block(32, 8);
-  const int64_t gx = (K + 31) / 32, gy = (R + 31) / 32;
-  const dim3 grid(static_cast<unsigned>(gx < 4096 ? (gx < 1 ? 1 : gx) : 4096),
-                  static_cast<unsigned>(gy < 4096 ? (gy < 1 ? 1 : gy) : 4096));
-  if (k_contig)
-    split3_kernel<true><<<grid, block, 0, s>>>(src, lds, dst, ldd, R, K, is_b);
-  else
-    split3_kernel<false><<<grid, block, 0, s>>>(src, lds, dst, ldd, R, K, is_b);
+  if (R <= 0 || K <= 0) return cudaSuccess;
+  if (k_contig) {
+    // 16-byte accesses: the source rows, the destination rows and the segment offsets K
+    // and 2K must all fall on 16-byte boundaries
+    const bool vec = reinterpret_cast<uintptr_t>(src) % 16 == 0 && lds % 4 == 0 &&
+                     reinterpret_cast<uintptr_t>(dst) % 16 == 0 && ldd % 4 == 0 && K % 4 == 0;
+    const int64_t chunks = R * ((K + 3) / 4);
+    const int64_t blocks = (chunks + 255) / 256;
+    split3_rows_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, s>>>(
+        src, lds, dst, ldd, R, K, is_b, vec);
+  } else {
+    const dim3 block(32, 8);
+    const int64_t gx = (R + 127) / 128, gy = (K + 31) / 32;
+    const dim3 grid(static_cast<unsigned>(gx < 4096 ? gx : 4096),
+                    static_cast<unsigned>(gy < 4096 ? gy : 4096));
+    split3_cols_kernel<<<grid, block, 0, s>>>(src, lds, dst, ldd, R, K, is_b);
+  }
   return cudaGetLastError();
 }
 
