@@ -257,15 +257,50 @@ __global__ void __launch_bounds__(kXThreads, 1)
       };
       WorkIter work(sched, cluster_id);
       SkSegment seg;
+      auto next_stage = [&]() {
+        if (++stage == G::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      };
       while (ok && work.next(seg)) {
         uint32_t d_tmem = 0;
-        int left = 0;  // per-MMA chunks: MMAs left in the current chunk (0: start one)
-        for (int kb = seg.kb_begin; ok && kb < seg.kb_end; ++kb) {
-          const int in_chunk = by_block ? (kb - seg.kb_begin) % chunk_kb : 0;
-          if (by_block && in_chunk == 0 && !take_acc(d_tmem)) {
-            ok = false;
-            break;
+        if (by_block) {
+          // chunk by chunk: a fresh accumulator, then a tight loop over its K-blocks
+          for (int c0 = seg.kb_begin; ok && c0 < seg.kb_end; c0 += chunk_kb) {
+            if (!take_acc(d_tmem)) {
+              ok = false;
+              break;
+            }
+            const int c1 = c0 + chunk_kb < seg.kb_end ? c0 + chunk_kb : seg.kb_end;
+            for (int kb = c0; kb < c1; ++kb) {
+              if (!mbar_wait_cluster(&full[stage], phase, wd)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
+              const uint32_t b_base = a_base + G::A_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < G::K_STEPS; ++kk) {
+                const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+                const uint32_t accumulate = (kb != c0) || kk != 0;
+                if (F16ACC)
+                  mma_f16_pair(d_tmem, ad, bd, p.idesc, accumulate);
+                else
+                  mma_tf32_pair(d_tmem, ad, bd, p.idesc, accumulate);
+              }
+              mma_commit_pair_multicast(&empty[stage], 0x3);
+              next_stage();
+            }
+            if (!ok) break;
+            hand_over();
           }
+          continue;
+        }
+        int left = 0;  // MMAs left in the current chunk (0: start one)
+        for (int kb = seg.kb_begin; ok && kb < seg.kb_end; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase, wd)) {
             ok = false;
             break;
@@ -274,46 +309,29 @@ __global__ void __launch_bounds__(kXThreads, 1)
           const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t b_base = a_base + G::A_BYTES;
           const bool last_kb = kb == seg.kb_end - 1;
-          if (by_block) {
 #pragma unroll
-            for (int kk = 0; kk < G::K_STEPS; ++kk) {
-              const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
-              const uint32_t accumulate = (in_chunk | kk) != 0;
-              if (F16ACC)
-                mma_f16_pair(d_tmem, ad, bd, p.idesc, accumulate);
-              else
-                mma_tf32_pair(d_tmem, ad, bd, p.idesc, accumulate);
+          for (int kk = 0; kk < G::K_STEPS; ++kk) {
+            const bool fresh = left == 0;
+            if (fresh) {
+              if (!take_acc(d_tmem)) {
+                ok = false;
+                break;
+              }
+              left = chunk;
             }
-            if (in_chunk == chunk_kb - 1 || last_kb) hand_over();
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < G::K_STEPS; ++kk) {
-              const bool fresh = left == 0;
-              if (fresh) {
-                if (!take_acc(d_tmem)) {
-                  ok = false;
-                  break;
-                }
-                left = chunk;
-              }
-              const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
-              if (F16ACC)
-                mma_f16_pair(d_tmem, ad, bd, p.idesc, fresh ? 0u : 1u);
-              else
-                mma_tf32_pair(d_tmem, ad, bd, p.idesc, fresh ? 0u : 1u);
-              if (--left == 0 || (last_kb && kk == G::K_STEPS - 1)) {
-                hand_over();
-                left = 0;
-              }
+            const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            if (F16ACC)
+              mma_f16_pair(d_tmem, ad, bd, p.idesc, fresh ? 0u : 1u);
+            else
+              mma_tf32_pair(d_tmem, ad, bd, p.idesc, fresh ? 0u : 1u);
+            if (--left == 0 || (last_kb && kk == G::K_STEPS - 1)) {
+              hand_over();
+              left = 0;
             }
           }
           mma_commit_pair_multicast(&empty[stage], 0x3);
-          if (++stage == G::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          next_stage();
         }
       }
       mma_commit_pair(drain);
