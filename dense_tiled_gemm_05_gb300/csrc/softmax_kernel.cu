@@ -130,39 +130,82 @@ __global__ void __launch_bounds__(T, 1024 / T) softmax_rows_kernel(const TI *__r
   }
 }
 
-// Rows longer than the register kernel holds: two passes over the row. The first keeps,
-// per thread, the maximum m of its values and l = sum exp(x - m), rescaling l whenever m
-// grows; the block then combines the (m, l) pairs. A NaN or +inf anywhere makes the row NaN
-// (the formula's x - m is NaN there); a row of -inf only gives NaN through -inf - -inf.
-template <typename TI, typename TO>
-__global__ void __launch_bounds__(1024) softmax_rows_online_kernel(const TI *__restrict__ X,
-                                                                   int64_t ldx, TO *__restrict__ Y,
-                                                                   int64_t ldy, int64_t M,
-                                                                   int64_t N) {
-  constexpr int T = 1024;
+// VEC consecutive values of a row from column j0 (16-byte load when the row is aligned and
+// the piece is whole); columns past N read as -inf.
+template <typename TI, bool VECTOR>
+__device__ __forceinline__ void load_piece(const TI *x, int64_t j0, int64_t N,
+                                           float (&v)[16 / sizeof(TI)]) {
+  constexpr int VEC = 16 / sizeof(TI);
+  if (VECTOR && j0 + VEC <= N) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(x + j0);
+    const TI *e = reinterpret_cast<const TI *>(&raw);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) v[i] = to_f32(e[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) v[i] = j0 + i < N ? to_f32(x[j0 + i]) : -INFINITY;
+  }
+}
+
+// Rows longer than the register kernel holds: two passes over the row (the second mostly
+// from L2: the rows in flight fit in it). The first keeps, per thread, the maximum m of its
+// values and l = sum exp(x - m), rescaling l whenever a piece raises m; the block then
+// combines the (m, l) pairs. A NaN or +inf anywhere makes the row NaN (the formula's x - m
+// is NaN there); a row of -inf only gives NaN through -inf - -inf. 512 threads, two CTAs
+// (two rows) per SM.
+template <typename TI, typename TO, bool VECTOR>
+__global__ void __launch_bounds__(512, 2) softmax_rows_online_kernel(const TI *__restrict__ X,
+                                                                     int64_t ldx,
+                                                                     TO *__restrict__ Y,
+                                                                     int64_t ldy, int64_t M,
+                                                                     int64_t N) {
+  constexpr int T = 512;
+  constexpr int VEC = 16 / sizeof(TI);
   __shared__ float red[32];
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const TI *x = X + row * ldx;
     float m = -INFINITY, l = 0.0f;
     bool bad = false;
-    for (int64_t j = threadIdx.x; j < N; j += T) {
-      const float xv = to_f32(x[j]);
-      if (xv != xv || xv == INFINITY) {
-        bad = true;
-      } else if (xv > m) {
-        l = l * expf(m - xv) + 1.0f;  // rescale the sum to the new maximum
-        m = xv;
-      } else if (xv != -INFINITY) {
-        l += expf(xv - m);
+    for (int64_t j0 = static_cast<int64_t>(threadIdx.x) * VEC; j0 < N;
+         j0 += static_cast<int64_t>(T) * VEC) {
+      float v[VEC];
+      load_piece<TI, VECTOR>(x, j0, N, v);
+      float pm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        bad |= v[i] != v[i] || v[i] == INFINITY;
+        pm = fmaxf(pm, v[i]);
       }
+      if (pm > m) {
+        l *= expf(m - pm);  // rescale the sum to the new maximum (0 while m is -inf)
+        m = pm;
+      }
+#pragma unroll
+      for (int i = 0; i < VEC; ++i)
+        if (v[i] != -INFINITY) l += expf(v[i] - m);
     }
     const float row_m = block_reduce<T, true>(m, red);
     const float lt = m == -INFINITY ? 0.0f : l * expf(m - row_m);
     const float row_l = block_reduce<T, false>(lt, red);
     const float mm = __syncthreads_or(bad) ? __int_as_float(0x7fffffff) : row_m;
     TO *y = Y + row * ldy;
-    for (int64_t j = threadIdx.x; j < N; j += T)
-      y[j] = from_f32<TO>(expf(to_f32(x[j]) - mm) / row_l);
+    for (int64_t j0 = static_cast<int64_t>(threadIdx.x) * VEC; j0 < N;
+         j0 += static_cast<int64_t>(T) * VEC) {
+      float v[VEC];
+      load_piece<TI, VECTOR>(x, j0, N, v);
+      if (VECTOR && j0 + VEC <= N && sizeof(TO) * VEC % 16 == 0) {
+        TO out[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) out[i] = from_f32<TO>(expf(v[i] - mm) / row_l);
+#pragma unroll
+        for (int w = 0; w < static_cast<int>(sizeof(TO) * VEC / 16); ++w)
+          reinterpret_cast<uint4 *>(y + j0)[w] = reinterpret_cast<const uint4 *>(out)[w];
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i)
+          if (j0 + i < N) y[j0 + i] = from_f32<TO>(expf(v[i] - mm) / row_l);
+      }
+    }
   }
 }
 
@@ -201,8 +244,12 @@ cudaError_t dispatch(const void *X, int64_t ldx, void *Y, int64_t ldy, int64_t M
   const int64_t rows_cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 64;
   const int grid = static_cast<int>(M < rows_cap ? M : rows_cap);
   if (chunks > 1024 * MAX_CH) {
-    softmax_rows_online_kernel<TI, TO><<<grid, 1024, 0, s>>>(
-        static_cast<const TI *>(X), ldx, static_cast<TO *>(Y), ldy, M, N);
+    if (vector)
+      softmax_rows_online_kernel<TI, TO, true><<<grid, 512, 0, s>>>(
+          static_cast<const TI *>(X), ldx, static_cast<TO *>(Y), ldy, M, N);
+    else
+      softmax_rows_online_kernel<TI, TO, false><<<grid, 512, 0, s>>>(
+          static_cast<const TI *>(X), ldx, static_cast<TO *>(Y), ldy, M, N);
     return cudaGetLastError();
   }
 #define SOFTMAX_TRY(T_)                                                                        \
