@@ -164,3 +164,22 @@ def test_f16acc_rejections(g):
     with pytest.raises(g.GemmError):
         h.matmul(f, f, precision="f16acc")
     h.close()
+
+
+def test_f16acc_bench_size_sampled(g):
+    """The measured fp16-accumulator workload (fp16 4096^3, N(0,1) * 0.1, chunk 16) in the
+    bench's launch configuration: sampled rows against the oracle's definition."""
+    p = W.f16acc_square(4096)
+    h = g.Gemm(0)
+    c = h.matmul(to_device(p.A), to_device(p.B), out_dtype="f16", precision="f16acc")
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    rows = [0, 255, 256, 2047, 4095, 1234]
+    sub = W.Problem("rows", p.A[rows], p.B, "f16", "f16acc")
+    ref = oracle_f16acc(sub, 16)
+    got = c[rows].cpu().double().numpy()
+    diff = np.abs(got - ref)
+    bound = 4 * f16_ulp(running_total_bound(sub, 16))
+    assert np.all(diff <= bound)
+    assert np.mean(diff == 0) >= 0.99
+    h.close()

@@ -118,3 +118,19 @@ def test_softmax_rejects_overlap(h):
     x = torch.randn(8, 64, device="cuda")
     with pytest.raises(g.GemmError):
         h.softmax_rows(x[:, :32], out=x[:, 16:48])
+
+
+def test_softmax_bench_size_sampled(h):
+    """The measured workload, 16384 x 8192 fp32 (N(0,1) * 3 entries, the bench's seed), in the
+    launch configuration the bench times: sampled rows against the oracle, and every row's
+    sum equal to 1 within fp32 rounding."""
+    import bench
+    x = bench.softmax_input(16384, 8192)
+    y = h.softmax_rows(x.cuda())
+    torch.cuda.synchronize()
+    rows = sorted(set([0, 1, 8191, 16383] + list(np.random.default_rng(5).integers(0, 16384, 60))))
+    ref = oracle.softmax_rows(x[rows].numpy().reshape(-1), len(rows), 8192, ldx=8192,
+                              x_dtype="f32")
+    check(y[rows], ref, "f32")
+    sums = y.double().sum(dim=1).cpu()
+    assert torch.all((sums - 1.0).abs() < 1e-4)
