@@ -372,18 +372,31 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const uint32_t t = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            acc * G::BN + half * G::COLS;
 #pragma unroll
-        for (int q = 0; q < G::COLS / 32; ++q) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t + q * 32, r);
-          tmem_wait_ld();
-          if (F16ACC) {
-            // partial = fp16(chunk dot); acc = fp16(acc + partial)
+        if (F16ACC) {
+          // two 32-column reads in flight per wait (the chunk's drain is this kernel's
+          // critical path when chunks are single MMAs); partial = fp16(chunk dot),
+          // acc = fp16(acc + partial)
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              hsum[q * 16 + j] = __hadd2(
-                  hsum[q * 16 + j],
-                  __floats2half2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])));
-          } else {
+          for (int q = 0; q < G::COLS / 32; q += 2) {
+            uint32_t r[2][32];
+            tmem_ld_32x32b_x32(t + q * 32, r[0]);
+            tmem_ld_32x32b_x32(t + (q + 1) * 32, r[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                hsum[(q + h2) * 16 + j] =
+                    __hadd2(hsum[(q + h2) * 16 + j],
+                            __floats2half2_rn(__uint_as_float(r[h2][2 * j]),
+                                              __uint_as_float(r[h2][2 * j + 1])));
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < G::COLS / 32; ++q) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t + q * 32, r);
+            tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) sum[q * 32 + j] += __uint_as_float(r[j]);
           }
