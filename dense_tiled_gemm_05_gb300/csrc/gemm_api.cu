@@ -90,10 +90,10 @@ GEMM_API void gemm_destroy(gemm_handle_t h) {
   if (h->sk_ws) cudaFree(h->sk_ws);
   if (h->hp_buf) cudaFree(h->hp_buf);
   if (h->st_buf) cudaFree(h->st_buf);
-  if (h->hp_ready) {
-    for (cudaStream_t st : h->hp_stream) cudaStreamDestroy(st);
-    for (cudaEvent_t ev : h->hp_event) cudaEventDestroy(ev);
-  }
+  for (cudaStream_t st : h->hp_stream)
+    if (st) cudaStreamDestroy(st);
+  for (cudaEvent_t ev : h->hp_event)
+    if (ev) cudaEventDestroy(ev);
   if (h->status) cudaFree(h->status);
   delete h;
 }

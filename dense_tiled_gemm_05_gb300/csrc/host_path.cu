@@ -37,10 +37,17 @@ int host_panels(int64_t extent, int64_t width, int64_t *start) {
 
 gemm_status_t host_pipeline_setup(gemm_handle_t h) {
   if (h->hp_ready) return GEMM_OK;
+  // (after a failure part of them exist: those are kept, the rest created on the next call)
   for (cudaStream_t &st : h->hp_stream)
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (!st && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+      st = nullptr;
+      return cuda_fail(cudaGetLastError(), "host pipeline streams");
+    }
   for (cudaEvent_t &ev : h->hp_event)
-    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (!ev && cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+      ev = nullptr;
+      return cuda_fail(cudaGetLastError(), "host pipeline events");
+    }
   h->hp_ready = true;
   return GEMM_OK;
 }
