@@ -60,9 +60,11 @@
  * handle owns.
  *
  * Threads and streams: a handle may be used from one host thread at a time.
- * Its workspace is reused by every call, so two calls on one handle that may
- * run concurrently on the GPU (different streams, no ordering) must not both
- * need the workspace; calls on a single stream are always safe.
+ * Its device buffers (staged operands, split-K partials, flags and epoch) are
+ * reused by every call, so the calls made on one handle must run one after
+ * another on the GPU: one stream, or streams ordered by events. Work that runs
+ * concurrently takes one handle per stream. (gemm_run_host orders its own
+ * internal streams.)
  */
 #ifndef GEMM_GB300_H
 #define GEMM_GB300_H
