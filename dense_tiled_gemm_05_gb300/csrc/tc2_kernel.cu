@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      const uint64_t keep = l2_policy_evict_last();  // operand tiles stay in L2 longest
       WorkIter work(sched, cluster_id);
       SkSegment seg;
       while (ok && work.next(seg)) {
@@ -139,20 +140,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (A_MN) {
 #pragma unroll
             for (int q = 0; q < G::BM / G::PANEL; ++q)
-              tma_load_2d_pair(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0);
+              tma_load_2d_pair_hint(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0,
+                                    keep);
           } else {
 #pragma unroll
             for (int j = 0; j < KPS; ++j)
-              tma_load_2d_pair(a_dst + j * G::A_BOX_BYTES, &tmA, fb, k0 + j * G::BOX_K, m0);
+              tma_load_2d_pair_hint(a_dst + j * G::A_BOX_BYTES, &tmA, fb, k0 + j * G::BOX_K, m0,
+                                    keep);
           }
           if (B_MN) {
 #pragma unroll
             for (int q = 0; q < G::BN_HALF / G::PANEL; ++q)
-              tma_load_2d_pair(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0);
+              tma_load_2d_pair_hint(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0,
+                                    keep);
           } else {
 #pragma unroll
             for (int j = 0; j < KPS; ++j)
-              tma_load_2d_pair(b_dst + j * G::B_BOX_BYTES, &tmB, fb, k0 + j * G::BOX_K, n0);
+              tma_load_2d_pair_hint(b_dst + j * G::B_BOX_BYTES, &tmB, fb, k0 + j * G::BOX_K, n0,
+                                    keep);
           }
           if (++stage == G::STAGES) {
             stage = 0;

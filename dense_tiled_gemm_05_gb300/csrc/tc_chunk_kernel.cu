@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      const uint64_t keep = l2_policy_evict_last();  // operand tiles stay in L2 longest
       WorkIter work(sched, cluster_id);
       SkSegment seg;
       while (ok && work.next(seg)) {
@@ -224,8 +225,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
           const uint32_t a_dst = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          tma_load_2d_pair(a_dst, &tmA, fb, kb * G::BK, m0);
-          tma_load_2d_pair(a_dst + G::A_BYTES, &tmB, fb, kb * G::BK, n0);
+          tma_load_2d_pair_hint(a_dst, &tmA, fb, kb * G::BK, m0, keep);
+          tma_load_2d_pair_hint(a_dst + G::A_BYTES, &tmB, fb, kb * G::BK, n0, keep);
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1;

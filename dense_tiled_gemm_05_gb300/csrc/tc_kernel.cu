@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      const uint64_t keep = l2_policy_evict_last();  // operand tiles stay in L2 longest
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         int pm, pn;
         tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
@@ -119,16 +120,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (A_MN) {
 #pragma unroll
             for (int q = 0; q < G::BM / G::PANEL; ++q)
-              tma_load_2d(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0);
+              tma_load_2d_hint(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0, keep);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, k0, m0);
+            tma_load_2d_hint(a_dst, &tmA, fb, k0, m0, keep);
           }
           if (B_MN) {
 #pragma unroll
             for (int q = 0; q < BN / G::PANEL; ++q)
-              tma_load_2d(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0);
+              tma_load_2d_hint(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0, keep);
           } else {
-            tma_load_2d(b_dst, &tmB, fb, k0, n0);
+            tma_load_2d_hint(b_dst, &tmB, fb, k0, n0, keep);
           }
           ++issued;
           if (++stage == G::STAGES) {
