@@ -32,7 +32,8 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
           6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_DEVICE"}
 OPTIONS = {"wait_timeout_us": 0, "force_path": 1, "group_m": 2, "max_ctas": 3,
            "fault_stall_producer": 4, "force_staging": 5, "cta_pair": 6,
-           "block_n": 7, "exact_chunk": 8, "stream_k": 9, "host_panel": 10, "acc_chunk": 11, "stage_k": 12}
+           "block_n": 7, "exact_chunk": 8, "stream_k": 9, "host_panel": 10, "acc_chunk": 11, "stage_k": 12,
+           "tile_rows": 13}
 PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma", 4: "tcgen05_3xtf32",
          5: "tcgen05_f16acc"}
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
@@ -57,7 +58,8 @@ class GemmError(RuntimeError):
 class TuneResult(ctypes.Structure):
     _fields_ = [("cta_pair", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("stream_k", ctypes.c_int32), ("stage_k", ctypes.c_int32),
-                ("group_m", ctypes.c_int32), ("candidates", ctypes.c_int32),
+                ("group_m", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
+                ("candidates", ctypes.c_int32),
                 ("best_us", ctypes.c_float), ("default_us", ctypes.c_float)]
 
     def as_dict(self):

@@ -39,6 +39,7 @@ struct gemm_handle_s {
   int exact_chunk = 0;  // 0 default
   int acc_chunk = 0;    // fp16-accumulator chunk in K elements, 0 default (16)
   int stage_k = 0;      // 128-byte K-blocks per stage of the CTA-pair kernel, 0 auto
+  int tile_rows = 0;    // rows of A per CTA of the CTA-pair kernel, 0 auto
   int stream_k = 0;     // 0 auto (on), 1 off
   int host_panel = 0;  // gemm_run_host panel width (rows of A, columns of B), 0 auto
   // split-K workspace of the CTA-pair kernel: partial tiles and flags
@@ -106,7 +107,7 @@ struct Problem {
 
 struct Options {
   int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
-  int stream_k = 0, exact_chunk = 0, acc_chunk = 0, stage_k = 0;
+  int stream_k = 0, exact_chunk = 0, acc_chunk = 0, stage_k = 0, tile_rows = 0;
 };
 
 // fp16-accumulator chunk (K elements per fp16 rounding of the running total) when the
@@ -141,6 +142,7 @@ struct Plan {
   int64_t acc_chunk;  // fp16 accumulator: K elements per rounding (0: fp32 accumulator)
   int group_m;        // raster group height (tile rows)
   int stream_k;       // GEMM_OPT_STREAM_K value the plan was made with
+  int cta_rows;       // rows of A per CTA (CTA-pair kernel: <= kTcBlockM; else kTcBlockM)
 };
 
 struct SplitK {

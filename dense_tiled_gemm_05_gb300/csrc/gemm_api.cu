@@ -133,6 +133,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->stage_k = static_cast<int>(v);
       return GEMM_OK;
+    case GEMM_OPT_TILE_ROWS:
+      if (v != 0 && (v < 64 || v > kTcBlockM || v % 8)) return GEMM_ERR_INVALID_ARG;
+      h->tile_rows = static_cast<int>(v);
+      return GEMM_OK;
     case GEMM_OPT_ACC_CHUNK:
       if (v < 0 || v > (int64_t{1} << 20) || v % 8) return GEMM_ERR_INVALID_ARG;
       h->acc_chunk = static_cast<int>(v);

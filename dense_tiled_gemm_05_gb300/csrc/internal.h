@@ -12,6 +12,8 @@ namespace gemm_gb300 {
 
 // Debug flags carried into the tensor-core kernel.
 enum : int { kDebugStallProducer = 1 };
+// TcParams::l2_once bits: the operand is read by one tile column (A) or row (B) only.
+enum : int { kL2OnceA = 1, kL2OnceB = 2 };
 
 // Output tile of the tensor-core kernel: 128 rows (one TMEM lane per row).
 constexpr int kTcBlockM = 128;
@@ -30,6 +32,9 @@ struct TcParams {
   uint64_t timeout_ns; // bounded-wait limit
   int32_t debug_flags;
   int32_t chunk_steps;    // chunked kernel: MMA instructions per TMEM partial sum
+  int32_t cta_rows;       // rows of A each CTA loads per tile (CTA-pair kernel; <= 128)
+  int32_t l2_once;        // kL2OnceA | kL2OnceB: operands loaded as first to evict from L2
+  int32_t k_rotate;       // whole tile t starts at K-block (t * k_rotate) mod k_blocks (0: 0)
   // split-K share of the last rounds (CTA-pair kernel; see sk_schedule.h)
   int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
   float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32

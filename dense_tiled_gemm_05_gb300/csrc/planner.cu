@@ -8,6 +8,7 @@
 // with cdiv(K, BLOCK_K) K-iterations per tile. Here the caller states M, N, K and the
 // leading dimensions explicitly, and the planner maps the same tile grid onto a
 // persistent schedule over the SMs.
+#include <cmath>
 #include <cstdint>
 
 #include "api_internal.h"
@@ -111,16 +112,40 @@ static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64
   return o;
 }
 
+// Tile slots of the CTA-pair kernel: one cluster of two SMs each, under the CTA cap.
+static int64_t pair_slots(int sm_count, int max_ctas) {
+  int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
+  if (max_ctas > 0 && max_ctas / 2 < clusters) clusters = max_ctas / 2 > 0 ? max_ctas / 2 : 1;
+  return clusters;
+}
+
 // Whether splitting the last rounds along K pays on GB300 (interleaved measurements of
 // bf16 products): it does when at least two whole rounds come first and every tile has a
 // long K-loop (4096^3 +5.6 %, 5120^3 +7.4 %, 8192^3 +3.6 %); it does not when every tile
 // has to be split (2048^3 -26 %) or K is short (8192 x 8192 x 2048 -1.6 %), where the
-// partial-tile traffic costs more than the idle tail it saves. stream_k: 0 by this rule,
-// 1 never, 2 whenever the schedule allows.
+// partial-tile traffic costs more than the idle tail it saves. The exception is a product
+// whose tiles would leave more than half of the slots idle, with long K-loops (128 or more
+// K-blocks): one tile's K-loop then sets the time, and sharing it out wins (bf16
+// M x 128 x 8192: M = 2048 22.7 against 34.4 us, 4096 24.9 against 35.1, 8192 33.1
+// against 35.2; 12288, with 48 tiles for 76 slots, loses 5 %; 128 x 4096 x 4096, 64
+// K-blocks, 27.1 against 24.9). stream_k: 0 by this rule, 1 never, 2 whenever the
+// schedule allows. k_blocks counts 128-byte K-blocks.
 bool use_split_k(int stream_k, int64_t tiles, int64_t k_blocks, int64_t slots) {
   if (stream_k == 1) return false;
   if (stream_k == 2) return true;
-  return slots > 0 && tiles % slots != 0 && tiles / slots >= 2 && k_blocks >= 64;
+  if (slots <= 0) return false;
+  return (tiles % slots != 0 && tiles / slots >= 2 && k_blocks >= 64) ||
+         (2 * tiles <= slots && k_blocks >= 128);
+}
+
+// Most pieces a tile is split into when its pieces fill otherwise idle clusters. The owner
+// adds every other piece's partial in turn, so the best count grows only as the square
+// root of the K-loop: about six for 128 K-blocks (bf16 256 x 256 x 8192: 27 us over 4 to 8
+// clusters, 127 us over 76; 1024 x 128 x 8192, 4 tiles: 20.8 us over 32 clusters, 29 over
+// 76), sixteen for 1024.
+static int64_t idle_split_pieces(int64_t k_blocks) {
+  const int64_t p = static_cast<int64_t>(std::sqrt(static_cast<double>(k_blocks) / 4.0) + 0.5);
+  return p < 2 ? 2 : p;
 }
 
 // Tile width by a wave-quantisation cost model: a persistent grid runs
@@ -152,6 +177,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   Plan pl{};
   pl.group_m = opt.group_m;
   pl.stream_k = opt.stream_k;
+  pl.cta_rows = kTcBlockM;
   gemm_plan_info_t &I = pl.info;
   if (P.M == 0 || P.N == 0) {
     I.path = GEMM_PATH_NONE;
@@ -212,10 +238,18 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // flop; a problem no taller than one 128-row tile keeps single-CTA tiles, and so does a
   // compute-bound one whose 128 x 256 single-CTA tiles all run at once (one round on the
   // SMs), where the pair's cross-SM handshakes cost more than they save (bf16 2048^3:
-  // 16.6 against 18.7 us). Bandwidth-bound ones keep pairs, for their wide stages.
+  // 16.6 against 18.7 us). Bandwidth-bound ones keep pairs, for their wide stages. So do
+  // products with so few tiles that even 128-wide pair tiles leave more than half of the
+  // clusters idle, when K is long: the split-K rule then shares each tile's K-loop out
+  // (bf16 1024 x 512 x 8192: 27.5 against 41.3 us on single-CTA tiles; 512 x 1024 x 16384:
+  // 34.4 against 78.1; 128 x 128 x 65536: 61.8 against 289).
   const int64_t single_tiles = ((P.M + kTcBlockM - 1) / kTcBlockM) * ((P.N + 255) / 256);
   const bool one_round = single_tiles <= sm_count && intensity >= 256.0;
-  pl.variant.pair = opt.cta_pair == 2 || (opt.cta_pair == 0 && P.M > kTcBlockM && !one_round);
+  const int64_t narrow_kb = (P.K + 128 / es - 1) / (128 / es);
+  const bool few_tiles = opt.stream_k != 1 && narrow_kb >= 128 &&
+                         2 * ((P.M + 255) / 256) * ((P.N + 127) / 128) <= pair_slots(sm_count, opt.max_ctas);
+  pl.variant.pair = opt.cta_pair == 2 ||
+                    (opt.cta_pair == 0 && ((P.M > kTcBlockM && !one_round) || few_tiles));
   pl.variant.block_n =
       opt.block_n ? opt.block_n
                   : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
@@ -234,14 +268,31 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // K-block per stage (4096^3 lost 9 % with wide stages). A forced split-K keeps narrow
   // K-blocks, the finer unit it shares out (one 256 x 256 x 8192 tile: 128 units for 76
   // clusters rather than 64).
+  // So does a product whose few tiles the split-K rule shares out over idle slots.
+  const bool rows_ok = pl.variant.pair && !chunked && !pl.a.mn_major;
+  if (opt.tile_rows && !rows_ok) return GEMM_ERR_UNSUPPORTED;
+  if (opt.tile_rows) pl.cta_rows = opt.tile_rows;
+  const int64_t clusters = pair_slots(sm_count, opt.max_ctas);
+  const int64_t pair_tiles = ((P.M + 2 * pl.cta_rows - 1) / (2 * pl.cta_rows)) *
+                             ((P.N + pl.variant.block_n - 1) / pl.variant.block_n);
+  const bool idle_split = pl.variant.pair && !chunked && 2 * pair_tiles <= clusters &&
+                          use_split_k(opt.stream_k, pair_tiles, narrow_kb, clusters);
   const bool wide_ok = pl.variant.pair && !chunked && es == 2 && !pl.a.mn_major && !pl.b.mn_major;
   if (opt.stage_k == 2 && !wide_ok) return GEMM_ERR_UNSUPPORTED;
-  pl.variant.kps =
-      opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < 256.0 && opt.stream_k != 2)
-          ? 2
-          : 1;
+  pl.variant.kps = opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < 256.0 &&
+                                        opt.stream_k != 2 && !idle_split)
+                       ? 2
+                       : 1;
+  // Rows of A per CTA of a pair tile (GEMM_OPT_TILE_ROWS; 128 by default). The MMA is
+  // always 128 rows per CTA; a CTA given fewer loads only those (the rest of its
+  // shared-memory rows feed accumulator lanes that are never stored). Shorter tiles do not
+  // pay by default: on bf16 M x 128 x 8192 the time stays that of one tile's K-loop, set by
+  // each SM's stream of A, whether 64 or 74 clusters run (M = 16384: 47.7 us with 256-row
+  // tiles, 50.5 us with 224), but two rounds of shorter tiles can beat one and a part
+  // (M = 24576: 71.8 us with 192-row tiles, 80.4 us with 256); gemm_tune tries them.
+  // (Set above, before the stage width.)
   I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : f16acc ? GEMM_PATH_TCGEN05_F16ACC : GEMM_PATH_TCGEN05;
-  I.tile_m = pl.variant.pair ? 2 * kTcBlockM : kTcBlockM;
+  I.tile_m = pl.variant.pair ? 2 * pl.cta_rows : kTcBlockM;
   I.tile_n = pl.variant.block_n;
   I.tile_k = pl.variant.kps * 128 / es;
   I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
@@ -266,13 +317,14 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   if (pl.variant.pair) {
     // One cluster of two CTAs per tile slot; the launch clamps to the clusters that fit.
     // With a split-K share every cluster takes part, even when there are fewer tiles.
-    int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
-    if (opt.max_ctas > 0 && opt.max_ctas / 2 < clusters) clusters = opt.max_ctas / 2 > 0 ? opt.max_ctas / 2 : 1;
     // (the fp16 accumulator never splits: its running total takes the chunks in order)
     const bool split = !pl.variant.f16acc && use_split_k(opt.stream_k, tiles, I.k_iters, clusters) &&
                        sk_dp_tiles(static_cast<int32_t>(tiles), static_cast<int32_t>(I.k_iters),
                                    static_cast<int32_t>(clusters), true) < tiles;
-    I.ctas = 2 * (split || tiles > clusters ? clusters : tiles);
+    // Tiles split over otherwise idle clusters take a limited number of pieces each.
+    const int64_t cap = idle_split_pieces(I.k_iters) * tiles;
+    const int64_t slots = split && 2 * tiles <= clusters && cap < clusters ? cap : clusters;
+    I.ctas = 2 * (split || tiles > clusters ? slots : tiles);
   } else {
     int64_t ctas = sm_count > 0 ? sm_count : 1;
     if (opt.max_ctas > 0 && opt.max_ctas < ctas) ctas = opt.max_ctas;
@@ -303,6 +355,7 @@ Options options_of(gemm_handle_t h) {
     o.exact_chunk = h->exact_chunk;
     o.acc_chunk = h->acc_chunk;
     o.stage_k = h->stage_k;
+    o.tile_rows = h->tile_rows;
   }
   return o;
 }
@@ -327,6 +380,7 @@ Options options_for(gemm_handle_t h, const Problem &P) {
     o.stream_k = t->choice.stream_k;
     o.stage_k = t->choice.stage_k;
     o.group_m = t->choice.group_m;
+    o.tile_rows = t->choice.tile_rows == kTcBlockM ? 0 : t->choice.tile_rows;
   }
   return o;
 }

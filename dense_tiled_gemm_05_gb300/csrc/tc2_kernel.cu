@@ -46,14 +46,17 @@ struct Cfg2 {
   static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int EPI_BYTES = kEpiWarps * 2 * kStoreBufBytes;
   static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 9;  // + one partial-load barrier per epilogue warp
   static constexpr int OWNER_SLICE = 48 * 1024;     // stage bytes an owner warp borrows
+  static constexpr int PART_BYTES = BN * 32 * 4;    // one partial's 32 rows, fp32
+  static constexpr int PART_BUFS = OWNER_SLICE / PART_BYTES;  // partial loads in flight
+  // + one partial-load barrier per buffer of each epilogue warp
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + kEpiWarps * PART_BUFS;
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(kEpiWarps * OWNER_SLICE <= STAGES * STAGE_BYTES, "owner slices fit the stages");
-  static_assert(BN * 32 * 4 <= OWNER_SLICE, "a warp's partial rows fit its slice");
+  static_assert(PART_BUFS >= 1 && PART_BUFS <= 3, "a warp's partial rows fit its slice");
   static_assert(KPS == 1 || (!A_MN && !B_MN), "wide stages for K-major operands only");
 };
 
@@ -72,8 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *tmem_full = empty + G::STAGES;
   uint64_t *tmem_empty = tmem_full + 2;
   uint64_t *drain = tmem_empty + 2;
-  uint64_t *part_bar = drain + 1;  // [kEpiWarps]: split-K partial loads of the owner warps
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(part_bar + kEpiWarps);
+  uint64_t *part_bar = drain + 1;  // [kEpiWarps][PART_BUFS]: owner warps' partial loads
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(part_bar + kEpiWarps * G::PART_BUFS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_empty[b], 2 * kEpiWarps);  // one arrive per epilogue warp, both CTAs
     }
     mbar_init(drain, 1);
-    for (int w = 0; w < kEpiWarps; ++w) mbar_init(&part_bar[w], 1);
+    for (int w = 0; w < kEpiWarps * G::PART_BUFS; ++w) mbar_init(&part_bar[w], 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -119,20 +122,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
-      const uint64_t keep = l2_policy_evict_last();  // operand tiles stay in L2 longest
+      // Operand tiles stay in L2 longest, unless only one tile row or column reads them.
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t pol_a = (p.l2_once & kL2OnceA) ? l2_policy_evict_first() : keep;
+      const uint64_t pol_b = (p.l2_once & kL2OnceB) ? l2_policy_evict_first() : keep;
+      // This CTA's rows of the tile (fewer than the MMA's 128 when the tiles were made
+      // shorter to occupy every cluster) and the bytes both CTAs load per stage.
+      const int rows = p.cta_rows;
+      const uint32_t stage_tx = 2u * static_cast<uint32_t>(rows * G::BK * ESIZE + G::B_BYTES);
       WorkIter work(sched, cluster_id);
       SkSegment seg;
       while (ok && work.next(seg)) {
         int pm, pn;
         tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
-        const int m0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM;
+        const int m0 = pm * (2 * rows) + static_cast<int>(rank) * rows;
         const int n0 = pn * G::BN + static_cast<int>(rank) * G::BN_HALF;
-        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+        // A piece may walk its K-blocks from any one of them, wrapping around: its sum
+        // takes the same set of K-blocks.
+        const int len = seg.kb_end - seg.kb_begin;
+        const int rot =
+            p.k_rotate ? static_cast<int>(static_cast<int64_t>(seg.tile) * p.k_rotate % len) : 0;
+        for (int i = 0; i < len; ++i) {
+          const int kb = seg.kb_begin + (i + rot < len ? i + rot : i + rot - len);
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t a_dst = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t b_dst = a_dst + G::A_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);  // the leader's barrier
@@ -141,23 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < G::BM / G::PANEL; ++q)
               tma_load_2d_pair_hint(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0,
-                                    keep);
+                                    pol_a);
           } else {
 #pragma unroll
             for (int j = 0; j < KPS; ++j)
               tma_load_2d_pair_hint(a_dst + j * G::A_BOX_BYTES, &tmA, fb, k0 + j * G::BOX_K, m0,
-                                    keep);
+                                    pol_a);
           }
           if (B_MN) {
 #pragma unroll
             for (int q = 0; q < G::BN_HALF / G::PANEL; ++q)
               tma_load_2d_pair_hint(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0,
-                                    keep);
+                                    pol_b);
           } else {
 #pragma unroll
             for (int j = 0; j < KPS; ++j)
               tma_load_2d_pair_hint(b_dst + j * G::B_BOX_BYTES, &tmB, fb, k0 + j * G::BOX_K, n0,
-                                    keep);
+                                    pol_b);
           }
           if (++stage == G::STAGES) {
             stage = 0;
@@ -227,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     WorkIter work(sched, cluster_id);
     SkSegment seg;
     const int e = warp - 2;       // epilogue warp index
-    uint32_t part_phase = 0;      // parity of this warp's partial-load barrier
+    uint32_t part_phase = 0;      // parities of this warp's partial-load barriers (bit b)
     bool ok = true;
     while (ok && work.next(seg)) {
       ok = mbar_wait_cluster(&tmem_full[acc], acc_phase, wd);
@@ -236,7 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int pm, pn;
       tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
-      const int row0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM + quarter * 32;
+      const int row0 = pm * (2 * p.cta_rows) + static_cast<int>(rank) * p.cta_rows + quarter * 32;
+      // Accumulator lanes of this warp that hold rows of the tile (all 32 unless the tile
+      // is shorter than the MMA).
+      const int valid = p.cta_rows - quarter * 32;
       const int n0 = pn * G::BN;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * G::BN;
       // First row of this warp's 32 rows in worker w's partial tile (row-major, BN columns).
@@ -257,29 +276,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The start of this tile was computed by workers first_src..last_src (all numbered
           // below this one): add their partials into the accumulator in increasing worker
           // order (a fixed order). The owner piece is its worker's last, so the pipeline
-          // stages are idle and each epilogue warp borrows a slice of them for the TMA loads.
+          // stages are idle and each epilogue warp borrows a slice of them: up to PART_BUFS
+          // partials are loaded ahead of the one being added.
           uint8_t *slice = smem + e * G::OWNER_SLICE;
-          for (int w = seg.first_src; ok && w <= seg.last_src; ++w) {
-            ok = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, epoch, wd);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+          uint64_t *bars = part_bar + e * G::PART_BUFS;
+          const int nsrc = seg.last_src - seg.first_src + 1;
+          // Wait for partial i's flag, then load it into buffer i % PART_BUFS.
+          auto fetch = [&](int i) {
+            const int w = seg.first_src + i;
+            bool f = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, epoch, wd);
+            f = __all_sync(0xffffffffu, f);
+            if (!f) return false;
             fence_proxy_async_global();
             if (lane == 0) {
-              mbar_arrive_expect_tx(&part_bar[e], G::BN * 32 * 4);
+              const int b = i % G::PART_BUFS;
+              uint8_t *buf = slice + b * G::PART_BYTES;
+              mbar_arrive_expect_tx(&bars[b], G::PART_BYTES);
 #pragma unroll
-              for (int b = 0; b < G::BN / 32; ++b)
-                tma_load_2d(smem_u32(slice + b * kStoreBufBytes), &tmP, smem_u32(&part_bar[e]),
-                            b * 32, part_row0(w));
+              for (int c = 0; c < G::BN / 32; ++c)
+                tma_load_2d(smem_u32(buf + c * kStoreBufBytes), &tmP, smem_u32(&bars[b]), c * 32,
+                            part_row0(w));
             }
-            ok = mbar_wait(&part_bar[e], part_phase, wd);
+            return true;
+          };
+          for (int i = 0; ok && i < nsrc && i < G::PART_BUFS; ++i) ok = fetch(i);
+          for (int i = 0; ok && i < nsrc; ++i) {
+            const int b = i % G::PART_BUFS;
+            ok = mbar_wait(&bars[b], (part_phase >> b) & 1u, wd);
             ok = __all_sync(0xffffffffu, ok);
-            part_phase ^= 1;
+            part_phase ^= 1u << b;
             if (!ok) break;
-            add_partial_into_tmem<G::BN>(t_row, slice, lane);
+            add_partial_into_tmem<G::BN>(t_row, slice + b * G::PART_BYTES, lane);
+            if (i + G::PART_BUFS < nsrc) {
+              __syncwarp();               // every lane has read buffer b
+              fence_proxy_async_smem();   // before the TMA unit writes it again
+              ok = fetch(i + G::PART_BUFS);
+            }
           }
           if (!ok) break;
         }
-        if (p.tma_store) {
+        if (valid <= 0) {
+          // no row of the tile in this warp's lanes
+        } else if (p.tma_store && valid >= 32) {
           if (p.out_dtype == GEMM_BF16)
             epilogue_tma<G::BN, GEMM_BF16>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
           else if (p.out_dtype == GEMM_F16)
@@ -287,12 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             epilogue_tma<G::BN, GEMM_F32>(&tmC, t_row, bufs, buf, lane, row0, n0, p.M, p.N);
         } else {
+          // plain stores; lanes past the tile's last row store nothing (row beyond C)
+          const int row = lane < valid ? row0 + lane : INT32_MAX;
           if (p.out_dtype == GEMM_BF16)
-            epilogue_direct<G::BN, GEMM_BF16>(p, t_row, row0 + lane, n0);
+            epilogue_direct<G::BN, GEMM_BF16>(p, t_row, row, n0);
           else if (p.out_dtype == GEMM_F16)
-            epilogue_direct<G::BN, GEMM_F16>(p, t_row, row0 + lane, n0);
+            epilogue_direct<G::BN, GEMM_F16>(p, t_row, row, n0);
           else
-            epilogue_direct<G::BN, GEMM_F32>(p, t_row, row0 + lane, n0);
+            epilogue_direct<G::BN, GEMM_F32>(p, t_row, row, n0);
         }
       }
       tc_fence_before();

@@ -102,12 +102,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
-      const uint64_t keep = l2_policy_evict_last();  // operand tiles stay in L2 longest
+      // Operand tiles stay in L2 longest, unless only one tile row or column reads them.
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t pol_a = (p.l2_once & kL2OnceA) ? l2_policy_evict_first() : keep;
+      const uint64_t pol_b = (p.l2_once & kL2OnceB) ? l2_policy_evict_first() : keep;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         int pm, pn;
         tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, pm, pn);
         const int m0 = pm * G::BM, n0 = pn * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        // the tile's K-loop may start at any K-block: the same K-blocks are summed
+        const int rot =
+            p.k_rotate ? static_cast<int>(static_cast<int64_t>(tile) * p.k_rotate % p.k_blocks) : 0;
+        for (int kb_i = 0; kb_i < p.k_blocks; ++kb_i) {
+          const int kb = kb_i + rot < p.k_blocks ? kb_i + rot : kb_i + rot - p.k_blocks;
           if (!mbar_wait(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
@@ -120,16 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (A_MN) {
 #pragma unroll
             for (int q = 0; q < G::BM / G::PANEL; ++q)
-              tma_load_2d_hint(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0, keep);
+              tma_load_2d_hint(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0, pol_a);
           } else {
-            tma_load_2d_hint(a_dst, &tmA, fb, k0, m0, keep);
+            tma_load_2d_hint(a_dst, &tmA, fb, k0, m0, pol_a);
           }
           if (B_MN) {
 #pragma unroll
             for (int q = 0; q < BN / G::PANEL; ++q)
-              tma_load_2d_hint(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0, keep);
+              tma_load_2d_hint(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0, pol_b);
           } else {
-            tma_load_2d_hint(b_dst, &tmB, fb, k0, n0, keep);
+            tma_load_2d_hint(b_dst, &tmB, fb, k0, n0, pol_b);
           }
           ++issued;
           if (++stage == G::STAGES) {

@@ -24,6 +24,7 @@ gemm_tune_result_t choice_of(const Options &o, const Plan &pl) {
   c.stream_k = o.stream_k;
   c.stage_k = pl.variant.kps;
   c.group_m = o.group_m;
+  c.tile_rows = pl.cta_rows;
   return c;
 }
 
@@ -53,26 +54,36 @@ GEMM_API gemm_status_t gemm_tune(gemm_handle_t h, int64_t M, int64_t N, int64_t 
   };
   std::vector<Cand> cands{{base, pl0}};
   if (pl0.info.path == GEMM_PATH_TCGEN05) {
+    // Shorter pair tiles (96 rows per CTA) only for bandwidth-bound products (under ~256
+    // flops per byte of A, B and C), where they can even out the rounds.
+    const int es = esize_of(in_dtype), os = esize_of(out_dtype);
+    const double intensity =
+        2.0 * M * N * K / (es * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
+                           static_cast<double>(os) * M * N);
+    const std::vector<int> rows_set = intensity < 256.0 ? std::vector<int>{0, 96} : std::vector<int>{0};
     for (int pair : {1, 2})
       for (int bn : {128, 256})
         for (int sk : {1, 2})
           for (int kps : {1, 2})
-            for (int gm : {4, 8, 16}) {
-              Options o = base;
-              o.cta_pair = pair, o.block_n = bn, o.stream_k = sk, o.stage_k = kps, o.group_m = gm;
-              Plan pl;
-              if (make_plan(P, o, h->sm_count, &pl) != GEMM_OK) continue;
-              const gemm_tune_result_t c = choice_of(o, pl);
-              bool dup = false;
-              for (const Cand &x : cands) {
-                const gemm_tune_result_t d = choice_of(x.o, x.pl);
-                // two plans differ if their tiles, stage width, raster group or split differ
-                dup |= d.cta_pair == c.cta_pair && d.block_n == c.block_n &&
-                       d.stage_k == c.stage_k && d.group_m == c.group_m &&
-                       (x.pl.info.split_tiles > 0) == (pl.info.split_tiles > 0);
+            for (int gm : {4, 8, 16})
+              for (int rows : rows_set) {
+                Options o = base;
+                o.cta_pair = pair, o.block_n = bn, o.stream_k = sk, o.stage_k = kps, o.group_m = gm;
+                o.tile_rows = rows;
+                Plan pl;
+                if (make_plan(P, o, h->sm_count, &pl) != GEMM_OK) continue;
+                const gemm_tune_result_t c = choice_of(o, pl);
+                bool dup = false;
+                for (const Cand &x : cands) {
+                  const gemm_tune_result_t d = choice_of(x.o, x.pl);
+                  // two plans differ if their tiles, stage width, raster group or split differ
+                  dup |= d.cta_pair == c.cta_pair && d.block_n == c.block_n &&
+                         d.stage_k == c.stage_k && d.group_m == c.group_m &&
+                         d.tile_rows == c.tile_rows &&
+                         (x.pl.info.split_tiles > 0) == (pl.info.split_tiles > 0);
+                }
+                if (!dup) cands.push_back({o, pl});
               }
-              if (!dup) cands.push_back({o, pl});
-            }
   }
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {

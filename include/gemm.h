@@ -191,9 +191,13 @@ typedef enum {
                                    last two panels' worth is cut in halves down to 256 */
   GEMM_OPT_ACC_CHUNK = 11,      /* GEMM_PREC_F16_ACC: K indices per fp16 rounding of the
                                    running total, a multiple of 8 (0 = default 16) */
-  GEMM_OPT_STAGE_K = 12         /* 128-byte K-blocks per pipeline stage of the CTA-pair
+  GEMM_OPT_STAGE_K = 12,        /* 128-byte K-blocks per pipeline stage of the CTA-pair
                                    kernel: 0 auto, 1, or 2 (K-major 16-bit operands only;
                                    otherwise GEMM_ERR_UNSUPPORTED at run time) */
+  GEMM_OPT_TILE_ROWS = 13       /* rows of A per CTA of the CTA-pair kernel (its tile has
+                                   twice as many): 0 = 128, or a multiple of 8 in [64, 128]
+                                   (K-major A and the fp32 accumulator only; otherwise
+                                   GEMM_ERR_UNSUPPORTED at run time) */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */
@@ -264,6 +268,7 @@ typedef struct {
   int32_t stream_k;   /* GEMM_OPT_STREAM_K value (0 auto, 1 never, 2 when possible) */
   int32_t stage_k;    /* GEMM_OPT_STAGE_K value (1 or 2) */
   int32_t group_m;    /* GEMM_OPT_GROUP_M value */
+  int32_t tile_rows;  /* GEMM_OPT_TILE_ROWS value (128 for single-CTA tiles) */
   int32_t candidates; /* configurations timed */
   float best_us;      /* mean time per product of the choice, microseconds */
   float default_us;   /* the same for the untuned plan (the first candidate) */
@@ -275,7 +280,7 @@ typedef struct {
  * `cuda_stream`, and keeps the fastest for the problem's signature (M, N, K, dtypes,
  * precision, layouts): later calls on this handle with that signature (gemm_run,
  * gemm_run_ex, gemm_plan, and the products inside gemm_run_strided and gemm_run_host)
- * use it in place of the handle's own values of those five options. The untuned plan is
+ * use it in place of the handle's own values of those six options. The untuned plan is
  * one of the candidates, so the choice is never slower as measured. Blocking: returns
  * after the last timing. It runs the real product, so C is written (with the product).
  * Problems that do not take the plain tensor-core path (exact fp32, the fp16 accumulator,

@@ -93,18 +93,33 @@ def test_plan_bf16_square_is_tcgen05_k_major():
     p = g.plan(t((16384, 8192), torch.bfloat16), t((8192, 128), torch.bfloat16, "col"),
                sm_count=148)
     assert (p["tile_m"], p["tile_n"], p["grid_m"], p["grid_n"]) == (256, 128, 64, 1)
+    assert p["ctas"] == 128 and p["split_tiles"] == 0
     # bandwidth-bound (125 flops per byte): two 128-byte K-blocks per stage, half the stages
     assert (p["tile_k"], p["k_iters"], p["stages"]) == (128, 64, 4)
     # A compute-bound problem whose single-CTA tiles all fit one round keeps single CTAs.
     p = g.plan(t((2048, 2048), torch.bfloat16), t((2048, 2048), torch.bfloat16, "col"),
                sm_count=148)
     assert p["cta_pair"] == 0 and (p["tile_m"], p["tile_n"], p["ctas"]) == (128, 256, 128)
-    # One 128-row tile of M: single-CTA tiles.
-    p = g.plan(t((128, 4096), torch.bfloat16), t((4096, 4096), torch.bfloat16, "col"),
+    # One 128-row tile of M with a short K: single-CTA tiles.
+    p = g.plan(t((128, 2048), torch.bfloat16), t((2048, 4096), torch.bfloat16, "col"),
                sm_count=148)
     # Fewer tiles than SMs: 32 tiles of 128 x 128 finish sooner than 16 of 128 x 256.
     assert p["cta_pair"] == 0 and (p["tile_m"], p["tile_n"], p["grid_m"]) == (128, 128, 1)
     assert p["ctas"] == 32
+    # The same with K = 8192 (128 K-blocks): so few tiles leave most SMs idle, so CTA pairs
+    # split each of the 16 tiles' K-loops over the idle clusters (six pieces a tile at
+    # most; 74 clusters here)
+    p = g.plan(t((128, 8192), torch.bfloat16), t((8192, 4096), torch.bfloat16, "col"),
+               sm_count=148)
+    assert p["cta_pair"] == 1 and (p["grid_m"], p["grid_n"]) == (1, 16)
+    assert p["split_tiles"] == 16 and p["ctas"] == 148 and p["tile_k"] == 64
+    # one tile: six pieces on six clusters for 128 K-blocks, sixteen for 1024
+    p = g.plan(t((256, 8192), torch.bfloat16), t((8192, 256), torch.bfloat16, "col"),
+               sm_count=148)
+    assert p["cta_pair"] == 1 and p["split_tiles"] == 1 and p["ctas"] == 12
+    p = g.plan(t((128, 65536), torch.bfloat16), t((65536, 128), torch.bfloat16, "col"),
+               sm_count=148)
+    assert p["cta_pair"] == 1 and p["split_tiles"] == 1 and p["ctas"] == 32
 
 
 def test_plan_row_major_b_is_mn_major():
@@ -220,3 +235,13 @@ def test_sources_share_nothing_with_the_oracle():
         if f.endswith((".c", ".py")):
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "dense_tiled_gemm_05_gb300" not in text and "gemm.h" not in text, f
+
+
+
+
+def test_plan_tile_rows_default():
+    """Rows per CTA of the pair kernel's tiles stay 128 unless the option asks otherwise
+    (GEMM_OPT_TILE_ROWS; its checks need a handle and run with the GPU tests)."""
+    for M, N, K in [(16384, 128, 8192), (24576, 128, 8192), (4096, 128, 8192), (5000, 100, 3000)]:
+        p = g.plan(t((M, K), torch.bfloat16), t((K, N), torch.bfloat16, "col"), sm_count=148)
+        assert p["cta_pair"] == 1 and p["tile_m"] == 256, (M, N, K)

@@ -29,6 +29,8 @@ def test_tune_keeps_the_fastest_and_applies_it(h):
     after = h.plan(a, b, out_dtype="f32")
     assert after["tile_n"] == r["block_n"] and after["cta_pair"] == (r["cta_pair"] == 2)
     assert after["tile_k"] == 64 * r["stage_k"]
+    assert after["tile_m"] == (2 * r["tile_rows"] if r["cta_pair"] == 2 else 128)
+    assert r["tile_rows"] == 128  # compute-bound: no shorter tiles tried
     # the tuned configuration computes the same exact integer product
     c = run_gpu(h, p)
     assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
@@ -39,6 +41,25 @@ def test_tune_keeps_the_fastest_and_applies_it(h):
     assert h.plan(qa, qb, out_dtype="f32") == g.Gemm(0).plan(qa, qb, out_dtype="f32")
     h.tune_clear()
     assert h.plan(a, b, out_dtype="f32") == before
+
+
+def test_tune_tries_shorter_pair_tiles(h):
+    # bandwidth-bound (bf16 6000 x 128 x 4096): 96-row CTAs are among the candidates
+    p = W.integer_problem(6000, 128, 4096, "bf16", seed=63, b_layout="col")
+    a, b = to_device(p.A), to_device(p.B)
+    r = h.tune(a, b, out_dtype="f32", iters=3)
+    assert r["tile_rows"] in (96, 128)
+    assert 0 < r["best_us"] <= r["default_us"]
+    after = h.plan(a, b, out_dtype="f32")
+    assert after["tile_m"] == (2 * r["tile_rows"] if r["cta_pair"] == 2 else 128)
+    c = run_gpu(h, p)
+    assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
+    # forcing 96 rows as the tuner would: the same exact product
+    h.tune_clear()
+    h.set_option("tile_rows", 96)
+    assert h.plan(a, b, out_dtype="f32")["tile_m"] == 192
+    c = run_gpu(h, p)
+    assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64))
 
 
 def test_tune_single_candidate_paths(h):
