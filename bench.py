@@ -42,10 +42,14 @@ METRIC = "GEMM TFLOP/s and % of GB300 dense tensor peak (1 GPU) vs CPU oracle"
 DATASHEET_BF16_TFLOPS = 2250.0  # dense bf16, NVIDIA GB300 (nominal)
 TF32_OVER_BF16 = 1100.0 / 2250.0  # nominal dense tf32 / bf16 ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE = os.path.join(ROOT, "profiles", "tc2_gemm_cta_pair_bf16_8192.md")
+# committed ncu summaries whose per-launch DRAM bytes the roofline's `traffic` reports
+PROFILES = {"bf16_8192": os.path.join(ROOT, "profiles", "tc2_gemm_cta_pair_bf16_8192.md"),
+            "bf16_skinny": os.path.join(ROOT, "profiles",
+                                        "tc2_gemm_cta_pair_bf16_skinny_16384x128x8192.md")}
 CSRC = os.path.join(ROOT, "dense_tiled_gemm_05_gb300", "csrc")
-# sources of the kernel the default workload runs (the CTA-pair tensor-core kernel)
-TC_SOURCES = [os.path.join(CSRC, f) for f in ("tc2_kernel.cu", "tc_common.cuh", "ptx.cuh")]
+# sources of the CTA-pair tensor-core kernel both run, and of the plan it is launched with
+TC_SOURCES = [os.path.join(CSRC, f) for f in ("tc2_kernel.cu", "tc_common.cuh", "ptx.cuh",
+                                              "sk_schedule.h", "planner.cu", "launch.cu")]
 
 
 def max_over_ranks(value, dist=None, device=None):
@@ -102,12 +106,13 @@ def algorithmic_bytes(p):
     return p.M * p.K * es + p.K * p.N * es + p.M * p.N * W.TORCH_DTYPES[p.out_dtype].itemsize
 
 
-def profile_traffic():
-    """dram bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
-    if not os.path.exists(PROFILE):
+def profile_traffic(workload):
+    """dram bytes per launch from the workload's committed ncu summary, if it was taken on
+    the current kernel and planner source (else None)."""
+    path = PROFILES.get(workload)
+    if path is None or not os.path.exists(path):
         return None
-    text = open(PROFILE).read()
+    text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not s:
@@ -584,7 +589,7 @@ def main():
         achieved = algorithmic_bytes(p) / (kernel_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": profile_traffic(args.workload),
                 "peak_source": "%s hbm_gbs (copy)" % peak_src}
     elif bound == "alu":
         props = torch.cuda.get_device_properties(dev)
@@ -616,7 +621,7 @@ def main():
                "%.2f s)" % (peak_src, elapsed_ms / 1e3) if long_run else
                "%s bf16_tflops (cuBLAS burst; timed region %.2f s)"
                % (peak_src, elapsed_ms / 1e3)) + src
-        traffic = profile_traffic() if args.workload == "bf16_8192" else None
+        traffic = profile_traffic(args.workload)
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": src,
                 "frac_of_burst": achieved / burst, "frac_of_sustained": achieved / sustained}
