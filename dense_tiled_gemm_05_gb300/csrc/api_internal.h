@@ -120,14 +120,16 @@ constexpr int kDefaultAccChunk = 16;
 // leading dimension), transposed into K-major form when it is an MN-major operand of a
 // kernel that reads K-major operands only (tf32, which the tensor cores take K-major only
 // on GB300, and the fp16-accumulator kernel), or split into tf32
-// hi/lo parts (exact-fp32 mode; always K-major, 3K columns).
+// hi/lo parts (exact-fp32 mode; always K-major: [hi | lo], each part K columns
+// zero-padded to split_kp, a whole number of 32-long K-blocks).
 struct OperandPlan {
   const void *ptr;          // caller's operand
   int64_t ld, outer, inner; // caller's storage: outer lines of inner elements
-  bool staged, transpose, split3;
+  bool staged, transpose, split_hl;
   bool is_b, k_contig;      // which operand; whether its storage is K-contiguous
   int64_t rows, k;          // logical rows (M or N) and K, for the split
   int64_t staged_ld;
+  int64_t split_kp;         // exact fp32: columns of each part (K rounded up to 32)
   size_t ws_offset, ws_bytes;
   // as read by the kernel (after staging)
   bool mn_major;

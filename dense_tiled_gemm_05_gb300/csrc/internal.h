@@ -35,6 +35,7 @@ struct TcParams {
   int32_t cta_rows;       // rows of A each CTA loads per tile (CTA-pair kernel; <= 128)
   int32_t l2_once;        // kL2OnceA | kL2OnceB: operands loaded as first to evict from L2
   int32_t k_rotate;       // whole tile t starts at K-block (t * k_rotate) mod k_blocks (0: 0)
+  int32_t split_kb;       // exact fp32: K-blocks per hi or lo part of the split operands
   // split-K share of the last rounds (CTA-pair kernel; see sk_schedule.h)
   int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
   float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32
@@ -111,11 +112,12 @@ cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld
 cudaError_t transpose_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t outer, int64_t inner, int esize, cudaStream_t s);
 
-// Exact-fp32 staging: writes the K-major operand [hi | hi | lo] (A) or [hi | lo | hi] (B)
-// of R rows and 3K columns (leading dim ldd >= 3K) from an fp32 operand X[r][k] stored
+// Exact-fp32 staging: writes the K-major operand [hi | lo] of R rows, each part K columns
+// zero-padded to Kp (a multiple of 32; leading dim ldd >= 2 Kp, a multiple of 4; dst
+// 16-byte aligned, else cudaErrorInvalidValue), from an fp32 operand X[r][k] stored
 // K-contiguous (src[r*lds + k]) or not (src[k*lds + r]).
-cudaError_t split3_launch(const float *src, int64_t lds, bool k_contig, float *dst, int64_t ldd,
-                          int64_t R, int64_t K, bool is_b, cudaStream_t s);
+cudaError_t split2_launch(const float *src, int64_t lds, bool k_contig, float *dst, int64_t ldd,
+                          int64_t R, int64_t K, int64_t Kp, cudaStream_t s);
 
 // dst[i * d0 + j * d1] = src[i * s0 + j * s1] for i < n0, j < n1 (element strides; the
 // source's may be 0). esize is 2 or 4 bytes.

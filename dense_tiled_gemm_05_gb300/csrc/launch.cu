@@ -110,9 +110,9 @@ static gemm_status_t ensure_workspace(gemm_handle_t h, size_t bytes) {
 }
 
 cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t s) {
-  if (o.split3)
-    return split3_launch(static_cast<const float *>(o.ptr), o.ld, o.k_contig,
-                         static_cast<float *>(dst), o.staged_ld, o.rows, o.k, o.is_b, s);
+  if (o.split_hl)
+    return split2_launch(static_cast<const float *>(o.ptr), o.ld, o.k_contig,
+                         static_cast<float *>(dst), o.staged_ld, o.rows, o.k, o.split_kp, s);
   if (o.transpose) return transpose_launch(o.ptr, o.ld, dst, o.staged_ld, o.outer, o.inner, es, s);
   return repack_launch(o.ptr, o.ld, dst, o.staged_ld, o.outer, o.inner, es, s);
 }
@@ -190,6 +190,7 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   tp.debug_flags = debug_flags;
   tp.chunk_steps = pl.chunk_steps;
   tp.cta_rows = pl.cta_rows;
+  tp.split_kb = pl.a.split_hl ? static_cast<int32_t>(pl.a.split_kp / 32) : 0;
   // An operand that only one tile column (A) or one tile row (B) reads is streamed once:
   // its loads go to L2 as first to evict, and whole tiles then start their K-loops at
   // staggered K-blocks, so that tiles running side by side do not all fetch the same

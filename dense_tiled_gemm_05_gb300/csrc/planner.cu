@@ -75,7 +75,7 @@ static bool tma_legal(const void *p, int64_t ld, int64_t outer, int es) {
 }
 
 static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout,
-                                bool k_is_rows_dim, int es, bool force_stage, bool split3,
+                                bool k_is_rows_dim, int es, bool force_stage, bool split_hl,
                                 bool k_major_only, size_t *ws_cursor) {
   OperandPlan o{};
   o.ptr = p;
@@ -91,13 +91,14 @@ static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64
   o.mn_major = !k_inner;
   o.k_outer = o.outer;
   o.k_inner = o.inner;
-  o.split3 = split3;
-  o.transpose = !split3 && o.mn_major && (es == 4 || k_major_only);
-  o.staged = split3 || o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
+  o.split_hl = split_hl;
+  o.transpose = !split_hl && o.mn_major && (es == 4 || k_major_only);
+  o.staged = split_hl || o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
   if (o.staged) {
-    if (split3) {
+    if (split_hl) {
+      o.split_kp = round_up(o.k, 32);  // 32 fp32 = one 128-byte K-block
       o.k_outer = o.rows;
-      o.k_inner = 3 * o.k;
+      o.k_inner = 2 * o.split_kp;
       o.mn_major = false;
     } else if (o.transpose) {
       o.k_outer = o.inner;
@@ -297,7 +298,8 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   I.tile_k = pl.variant.kps * 128 / es;
   I.grid_m = (P.M + I.tile_m - 1) / I.tile_m;
   I.grid_n = (P.N + I.tile_n - 1) / I.tile_n;
-  const int64_t k_total = split ? 3 * P.K : P.K;  // split operands concatenate 3 products
+  // split operands: three products over each part's padded K
+  const int64_t k_total = split ? 3 * pl.a.split_kp : P.K;
   I.k_iters = (k_total + I.tile_k - 1) / I.tile_k;
   if (I.grid_m * I.grid_n > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   // chunked kernel: four MMAs per 128-byte K-block

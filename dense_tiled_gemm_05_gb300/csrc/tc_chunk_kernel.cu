@@ -9,9 +9,10 @@
 // into their registers.
 //
 // * Exact fp32 ("Triton matmul", "Precision": fp32 inputs need an explicit choice between
-//   tf32 and full fp32 accuracy) on the tf32 tensor cores: split_kernel.cu writes
-//   A' = [hi(A) | hi(A) | lo(A)] and B' = [hi(B) ; lo(B) ; hi(B)] so that A' B' holds the
-//   three significant partial products of the split operands. The tensor cores' fp32
+//   tf32 and full fp32 accuracy) on the tf32 tensor cores: split_kernel.cu writes each
+//   operand as [hi | lo], and the producer walks the K-blocks of
+//   A' = [hi(A) | hi(A) | lo(A)] and B' = [hi(B) ; lo(B) ; hi(B)] by picking the part for
+//   each, so that A' B' holds the three significant partial products of the split operands. The tensor cores' fp32
 //   accumulation over a long K drifts (measured on GB300: 4e-6 of sum |a b| at K = 4096,
 //   growing with K), so no TMEM accumulator runs over more than a short chunk, and the
 //   chunks are summed in fp32 registers with ordinary IEEE adds; rounded once at the store.
@@ -225,8 +226,15 @@ __global__ void __launch_bounds__(kXThreads, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
           const uint32_t a_dst = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          tma_load_2d_pair_hint(a_dst, &tmA, fb, kb * G::BK, m0, keep);
-          tma_load_2d_pair_hint(a_dst + G::A_BYTES, &tmB, fb, kb * G::BK, n0, keep);
+          int xa = kb * G::BK, xb = xa;  // K coordinates of the A and B boxes
+          if (!F16ACC) {
+            // K-block j of product q reads A's part (q == 2 ? lo : hi), B's (q == 1 ? lo : hi)
+            const int q = kb / p.split_kb, j = kb - q * p.split_kb;
+            xa = (j + (q == 2 ? p.split_kb : 0)) * G::BK;
+            xb = (j + (q == 1 ? p.split_kb : 0)) * G::BK;
+          }
+          tma_load_2d_pair_hint(a_dst, &tmA, fb, xa, m0, keep);
+          tma_load_2d_pair_hint(a_dst + G::A_BYTES, &tmB, fb, xb, n0, keep);
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1;

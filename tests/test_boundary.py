@@ -160,12 +160,17 @@ def test_plan_fp32_modes():
                precision="tf32")
     assert p["stage_a"] == 1 and p["a_mn_major"] == 0 and p["stage_b"] == 0
     for prec in ("exact", "default"):
-        # Exact fp32: both operands split into tf32 hi/lo parts, 3K-long products.
+        # Exact fp32: both operands split into tf32 [hi | lo] parts (2K columns each), read
+        # as three K-long products.
         p = g.plan(a, b, precision=prec)
         assert p["path"] == "tcgen05_3xtf32" and p["tile_k"] == 32 and p["k_iters"] == 384
         assert p["stage_a"] == 1 and p["stage_b"] == 1
         assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
-        assert p["workspace_bytes"] == 2 * 4096 * 3 * 4096 * 4
+        assert p["workspace_bytes"] == 2 * 4096 * 2 * 4096 * 4
+    # a ragged K pads each part to whole 32-long K-blocks: K = 1000 -> 1024 per part
+    p = g.plan(t((300, 1000), torch.float32), t((1000, 200), torch.float32), precision="exact")
+    assert p["path"] == "tcgen05_3xtf32" and p["k_iters"] == 3 * 32
+    assert p["workspace_bytes"] == 300 * 2048 * 4 + 200 * 2048 * 4 + (256 - 300 * 2048 * 4 % 256) % 256
     p = g.plan(t((16, 16), torch.float32), t((16, 16), torch.float32))
     assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (4, 4, 4)
 
