@@ -47,9 +47,9 @@ PROFILES = {"bf16_8192": os.path.join(ROOT, "profiles", "tc2_gemm_cta_pair_bf16_
             "bf16_skinny": os.path.join(ROOT, "profiles",
                                         "tc2_gemm_cta_pair_bf16_skinny_16384x128x8192.md")}
 CSRC = os.path.join(ROOT, "dense_tiled_gemm_05_gb300", "csrc")
-# sources of the CTA-pair tensor-core kernel both run, and of the plan it is launched with
+# sources of the CTA-pair tensor-core kernel both workloads run
 TC_SOURCES = [os.path.join(CSRC, f) for f in ("tc2_kernel.cu", "tc_common.cuh", "ptx.cuh",
-                                              "sk_schedule.h", "planner.cu", "launch.cu")]
+                                              "sk_schedule.h")]
 
 
 def max_over_ranks(value, dist=None, device=None):
@@ -108,7 +108,7 @@ def algorithmic_bytes(p):
 
 def profile_traffic(workload):
     """dram bytes per launch from the workload's committed ncu summary, if it was taken on
-    the current kernel and planner source (else None)."""
+    the current kernel source (else None)."""
     path = PROFILES.get(workload)
     if path is None or not os.path.exists(path):
         return None
