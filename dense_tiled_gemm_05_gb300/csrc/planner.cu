@@ -121,22 +121,27 @@ static int64_t pair_slots(int sm_count, int max_ctas) {
 }
 
 // Whether splitting the last rounds along K pays on GB300 (interleaved measurements of
-// bf16 products): it does when at least two whole rounds come first and every tile has a
-// long K-loop (4096^3 +5.6 %, 5120^3 +7.4 %, 8192^3 +3.6 %); it does not when every tile
-// has to be split (2048^3 -26 %) or K is short (8192 x 8192 x 2048 -1.6 %), where the
-// partial-tile traffic costs more than the idle tail it saves. The exception is a product
-// whose tiles would leave more than half of the slots idle, with long K-loops (128 or more
+// bf16 products). The split share is the last whole round plus the partial one, r of a
+// round's worth of tiles with 1 < r < 2 (sk_schedule.h); split, those run about 1.1-1.3
+// times slower per tile than whole tiles (partial stores, owners' sums), so sharing them
+// out beats the two rounds they otherwise take while r is at most 1.6: 2560^2 x 8192
+// (r = 1.32) 66.2 against 84.4 us, 4096^3 (1.37) +5.8 %, 5120^3 (1.26) +7.4 %, 8192^3
+// (1.47) +3.6 %; 6144^2 x 4096 (1.58) even; 2048 x 4096 x 4096 (1.68) even; 3072^2 x 4096
+// (1.89) -7 %. K must be long enough (8192 x 8192 x 2048, 32 K-blocks, -1.6 %), and a
+// product with fewer tiles than slots keeps them whole (2048^2 x 8192 -6 %) unless its
+// tiles would leave more than half of the slots idle with a long K-loop (128 or more
 // K-blocks): one tile's K-loop then sets the time, and sharing it out wins (bf16
 // M x 128 x 8192: M = 2048 22.7 against 34.4 us, 4096 24.9 against 35.1, 8192 33.1
-// against 35.2; 12288, with 48 tiles for 76 slots, loses 5 %; 128 x 4096 x 4096, 64
-// K-blocks, 27.1 against 24.9). stream_k: 0 by this rule, 1 never, 2 whenever the
-// schedule allows. k_blocks counts 128-byte K-blocks.
+// against 35.2; 128 x 4096 x 4096, 64 K-blocks, 27.1 against 24.9). stream_k: 0 by this
+// rule, 1 never, 2 whenever the schedule allows. k_blocks counts 128-byte K-blocks.
 bool use_split_k(int stream_k, int64_t tiles, int64_t k_blocks, int64_t slots) {
   if (stream_k == 1) return false;
   if (stream_k == 2) return true;
   if (slots <= 0) return false;
-  return (tiles % slots != 0 && tiles / slots >= 2 && k_blocks >= 64) ||
-         (2 * tiles <= slots && k_blocks >= 128);
+  if (2 * tiles <= slots) return k_blocks >= 128;
+  if (tiles <= slots || tiles % slots == 0 || k_blocks < 64) return false;
+  const int64_t shared = tiles - (tiles / slots - 1) * slots;  // r * slots
+  return 10 * shared <= 16 * slots;
 }
 
 // Most pieces a tile is split into when its pieces fill otherwise idle clusters. The owner
@@ -151,10 +156,11 @@ static int64_t idle_split_pieces(int64_t k_blocks) {
 
 // Tile width by a wave-quantisation cost model: a persistent grid runs
 // ceil(tiles / slots) rounds, each as long as one tile. A 128-wide tile has half the
-// flops of a 256-wide one but, measured on GB300, takes about 0.75 of its time (every MMA
-// re-reads its 128 x 16 slice of A from shared memory, so narrow MMAs are starved of
-// shared-memory bandwidth); it wins only when it fills the machine much better, e.g.
-// when N itself is at most 128.
+// flops of a 256-wide one but, measured on GB300, takes about 0.8 of its time (0.74 on
+// bf16 2048^2 x 8192, 0.82 on 2560^2 x 8192, both split along K; every MMA re-reads its
+// 128 x 16 slice of A from shared memory, so narrow MMAs are starved of shared-memory
+// bandwidth); it wins only when it fills the machine much better, e.g. when N itself is
+// at most 128.
 static int pick_block_n(int64_t M, int64_t N, int64_t k_blocks, bool pair, int stream_k, int sm_count) {
   const int64_t rows = pair ? 2 * kTcBlockM : kTcBlockM;
   const int64_t slots = pair ? (sm_count > 1 ? sm_count / 2 : 1) : (sm_count > 0 ? sm_count : 1);
@@ -169,7 +175,7 @@ static int pick_block_n(int64_t M, int64_t N, int64_t k_blocks, bool pair, int s
                                 : static_cast<double>((tiles + slots - 1) / slots);
     return rounds * static_cast<double>(bn) * per_column;
   };
-  return cost(128, 1.5) < cost(256, 1.0) ? 128 : 256;
+  return cost(128, 1.6) < cost(256, 1.0) ? 128 : 256;
 }
 
 gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan *out) {
@@ -238,15 +244,17 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // CTA pairs (256-row tiles on two SMs) halve the shared-memory and L2 traffic per
   // flop; a problem no taller than one 128-row tile keeps single-CTA tiles, and so does a
   // compute-bound one whose 128 x 256 single-CTA tiles all run at once (one round on the
-  // SMs), where the pair's cross-SM handshakes cost more than they save (bf16 2048^3:
-  // 16.6 against 18.7 us). Bandwidth-bound ones keep pairs, for their wide stages. So do
+  // SMs) with a short K-loop, where the pair's cross-SM handshakes cost more than they
+  // save (bf16 2048^3: 17.1 against 19.0 us); from 64 K-blocks on, pairs win again (bf16
+  // 2048^2 x 4096: 27.7 against 29.4 us; 2048^2 x 8192: 46.3 against 53.0). Bandwidth-bound
+  // ones keep pairs, for their wide stages. So do
   // products with so few tiles that even 128-wide pair tiles leave more than half of the
   // clusters idle, when K is long: the split-K rule then shares each tile's K-loop out
   // (bf16 1024 x 512 x 8192: 27.5 against 41.3 us on single-CTA tiles; 512 x 1024 x 16384:
   // 34.4 against 78.1; 128 x 128 x 65536: 61.8 against 289).
   const int64_t single_tiles = ((P.M + kTcBlockM - 1) / kTcBlockM) * ((P.N + 255) / 256);
-  const bool one_round = single_tiles <= sm_count && intensity >= 256.0;
   const int64_t narrow_kb = (P.K + 128 / es - 1) / (128 / es);
+  const bool one_round = single_tiles <= sm_count && intensity >= 256.0 && narrow_kb < 64;
   const bool few_tiles = opt.stream_k != 1 && narrow_kb >= 128 &&
                          2 * ((P.M + 255) / 256) * ((P.N + 127) / 128) <= pair_slots(sm_count, opt.max_ctas);
   pl.variant.pair = opt.cta_pair == 2 ||
