@@ -250,3 +250,31 @@ def test_plan_tile_rows_default():
     for M, N, K in [(16384, 128, 8192), (24576, 128, 8192), (4096, 128, 8192), (5000, 100, 3000)]:
         p = g.plan(t((M, K), torch.bfloat16), t((K, N), torch.bfloat16, "col"), sm_count=148)
         assert p["cta_pair"] == 1 and p["tile_m"] == 256, (M, N, K)
+
+
+def test_plan_split_k_rule():
+    """Split-K shares out the last whole round plus the partial one when that is at most
+    1.6 rounds' worth of tiles (and K has >= 64 K-blocks); few-tile long-K products split
+    over idle clusters; compute-bound products take CTA pairs from 64 K-blocks on."""
+    def plan(M, N, K, sms):
+        return g.plan(t((M, K), torch.bfloat16), t((K, N), torch.bfloat16, "col"), sm_count=sms)
+    # 100 tiles on 76 clusters: 1.32 rounds shared
+    assert plan(2560, 2560, 8192, 152)["split_tiles"] == 100
+    # 144 tiles: 1.89 rounds, kept whole
+    assert plan(3072, 3072, 4096, 152)["split_tiles"] == 0
+    # 8192^3: 1024 tiles; on 76 clusters the last 112 tiles (1.47 rounds) are shared, on 74
+    # the last 136 (1.84) are not
+    assert plan(8192, 8192, 8192, 152)["split_tiles"] == 112
+    assert plan(8192, 8192, 8192, 148)["split_tiles"] == 0
+    # short K (32 K-blocks): never
+    assert plan(8192, 8192, 2048, 152)["split_tiles"] == 0
+    # fewer tiles than clusters but more than half: whole tiles
+    p = plan(2048, 2048, 8192, 152)
+    assert p["cta_pair"] == 1 and p["split_tiles"] == 0 and p["ctas"] == 128
+    # compute-bound, all single-CTA tiles in one round: single CTAs for 32 K-blocks, pairs
+    # from 64 on
+    assert plan(2048, 2048, 2048, 152)["cta_pair"] == 0
+    assert plan(2048, 2048, 4096, 152)["cta_pair"] == 1
+    # 2560^2: 256-wide tiles (128-wide ones cost 0.8 of a 256-wide one's time, too much
+    # for the rounds they save)
+    assert plan(2560, 2560, 8192, 152)["tile_n"] == 256
