@@ -261,6 +261,18 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Programmatic dependent launch. A grid launched with programmatic stream serialization
+// may start before the previous kernel on its stream has finished; griddepcontrol.wait
+// blocks until every grid it depends on has completed and its memory is visible (at once
+// when there is none). launch_dependents lets the next such grid on the stream be
+// scheduled onto SMs as this one's CTAs leave them.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // All threads of every CTA in the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::

@@ -109,6 +109,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers of both CTAs initialised; TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touches only this CTA's own resources, so it may overlap the end of
+  // the previous kernel on the stream; from here on global memory is read and written.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
   const int cluster_id = blockIdx.x / 2;
   const int num_clusters = gridDim.x / 2;
@@ -371,17 +375,21 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // The prologue (barriers, TMEM, tensor-map prefetch) may overlap the previous kernel's
+  // tail; the kernel waits for it before touching global memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = G::SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmP, p);
 }
 

@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above may overlap the previous kernel on the stream (the operand split
+  // copies, in exact mode); global memory only from here on.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
   const int cluster_id = blockIdx.x / 2;
   const int num_clusters = gridDim.x / 2;
@@ -535,8 +539,11 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
   cudaError_t e = cudaFuncSetAttribute(
       tc_chunk_kernel<F16ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgX<F16ACC>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = chunk_config<F16ACC>(grid, s, attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dependency_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, tc_chunk_kernel<F16ACC>, tmA, tmB, tmC, tmP, p);
 }
 

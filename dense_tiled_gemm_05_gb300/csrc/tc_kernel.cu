@@ -93,6 +93,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above may overlap the previous kernel on the stream; global memory only
+  // from here on.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
   const int num_tiles = p.tiles_m * p.tiles_n;
   uint32_t issued = 0;  // stage fills issued by the producer lane
@@ -258,8 +262,17 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, G::SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dependency_wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, p);
 }
 
 template <int ESIZE, int BN>
