@@ -131,12 +131,15 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(
   int sms = 0;
   st = noalloc_setup(dev, &scratch, &sms);
   if (st != GEMM_OK) return st;
-  st = make_plan(P, Options(), sms, &pl);
+  // Split-K keeps its partial tiles in a handle-owned workspace: plan whole tiles only.
+  Options whole;
+  whole.stream_k = 1;
+  st = make_plan(P, whole, sms, &pl);
   if (st != GEMM_OK) return st;
   if (pl.info.path == GEMM_PATH_TCGEN05_3XTF32 &&
       static_cast<size_t>(pl.info.workspace_bytes) > GEMM_NOALLOC_SCRATCH_BYTES - kStaticStatusBytes) {
     // Exact fp32 whose split operands do not fit the array: the fp32 FMA kernel needs none.
-    Options fma;
+    Options fma = whole;
     fma.force_path = 2;
     st = make_plan(P, fma, sms, &pl);
     if (st != GEMM_OK) return st;

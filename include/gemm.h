@@ -382,7 +382,9 @@ GEMM_API const char *gemm_version(void);
  * array of GEMM_NOALLOC_SCRATCH_BYTES that every GPU loading this library keeps until the
  * process exits. A call whose staged copies would not fit returns GEMM_ERR_UNSUPPORTED
  * before launching anything; use gemm_run_ex for it. Arguments and layouts are those of
- * gemm_run_ex; the device is the caller's current device; default options apply.
+ * gemm_run_ex; the device is the caller's current device; default options apply, except
+ * that tiles are never split along K (GEMM_OPT_STREAM_K = 1: split-K's partial tiles
+ * live in a handle's workspace).
  *
  * The first call on each device does a one-time set-up with that device current (it looks
  * up the array's device address and the SM count); make that first call before any
