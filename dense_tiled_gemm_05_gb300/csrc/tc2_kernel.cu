@@ -18,6 +18,12 @@
 // A stage holds KPS consecutive 128-byte K-blocks of each K-major operand (KPS = 1 or 2):
 // with 2, every row of A and B is fetched 256 contiguous bytes at a time, which keeps more
 // of each DRAM page's bytes in one request stream when the product is bandwidth-bound.
+//
+// Schedule options carried in TcParams: a CTA may load fewer than 128 rows of A
+// (cta_rows; the surplus accumulator lanes are never stored); an operand read by one tile
+// row or column only is loaded as first to evict from L2, and every piece of a K-loop
+// then starts at a staggered K-block (k_rotate); pieces of tiles split along K hand their
+// fp32 sums to the tile's owner through the workspace (sk_schedule.h).
 #include "tc_common.cuh"
 
 namespace gemm_gb300 {
@@ -130,8 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t keep = l2_policy_evict_last();
       const uint64_t pol_a = (p.l2_once & kL2OnceA) ? l2_policy_evict_first() : keep;
       const uint64_t pol_b = (p.l2_once & kL2OnceB) ? l2_policy_evict_first() : keep;
-      // This CTA's rows of the tile (fewer than the MMA's 128 when the tiles were made
-      // shorter to occupy every cluster) and the bytes both CTAs load per stage.
+      // This CTA's rows of the tile (fewer than the MMA's 128 under GEMM_OPT_TILE_ROWS)
+      // and the bytes both CTAs load per stage.
       const int rows = p.cta_rows;
       const uint32_t stage_tx = 2u * static_cast<uint32_t>(rows * G::BK * ESIZE + G::B_BYTES);
       WorkIter work(sched, cluster_id);

@@ -104,8 +104,9 @@ __device__ __forceinline__ void epilogue_tma(const CUtensorMap *tmC, uint32_t t_
   }
 }
 
-// Epilogue, direct form for a C that TMA cannot address (misaligned base or ldc): each
-// lane owns one row and writes its in-range columns with plain stores.
+// Epilogue, direct form for a C that TMA cannot address (misaligned base or ldc), and for
+// the warp a shortened tile ends in: each lane owns one row and writes its in-range
+// columns with plain stores (a lane given a row at or past M stores nothing).
 template <int BN, int OUT>
 __device__ __forceinline__ void epilogue_direct(const TcParams &p, uint32_t t_row, int row, int n0) {
   using T = typename std::conditional<OUT == GEMM_F32, float,

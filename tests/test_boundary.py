@@ -170,7 +170,10 @@ def test_plan_fp32_modes():
     # a ragged K pads each part to whole 32-long K-blocks: K = 1000 -> 1024 per part
     p = g.plan(t((300, 1000), torch.float32), t((1000, 200), torch.float32), precision="exact")
     assert p["path"] == "tcgen05_3xtf32" and p["k_iters"] == 3 * 32
-    assert p["workspace_bytes"] == 300 * 2048 * 4 + 200 * 2048 * 4 + (256 - 300 * 2048 * 4 % 256) % 256
+    assert p["workspace_bytes"] == (300 + 200) * 2048 * 4
+    # K = 1100 -> 1120 per part
+    p = g.plan(t((300, 1100), torch.float32), t((1100, 200), torch.float32), precision="exact")
+    assert p["workspace_bytes"] == 300 * 2240 * 4 + (256 - 300 * 2240 * 4 % 256) % 256 + 200 * 2240 * 4
     p = g.plan(t((16, 16), torch.float32), t((16, 16), torch.float32))
     assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (4, 4, 4)
 
