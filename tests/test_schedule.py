@@ -91,3 +91,27 @@ def test_headline_shapes():
     # tiles that fill whole rounds need no split.
     assert all(not segs for _, segs in check(152, 64, 76))
     assert g.lib().gemm_schedule_segments(4, 0, 2, 1, 0, None, None, 0) == -1
+
+
+def test_idle_split_pieces_per_tile():
+    # Few tiles with long K-loops are split over as many clusters as the planner gives
+    # them (about sqrt(K-blocks / 4) pieces a tile): every unit once, and no owner gathers
+    # more than that many partials less one.
+    import torch
+
+    def t(shape, layout="row"):
+        if layout == "row":
+            return torch.empty(shape, dtype=torch.bfloat16)
+        return torch.empty(shape[::-1], dtype=torch.bfloat16).t()
+
+    for M, N, K, cap in [(256, 256, 8192, 6), (1024, 128, 8192, 6), (128, 128, 32768, 11),
+                         (128, 128, 65536, 16)]:
+        p = g.plan(t((M, K)), t((K, N), "col"), sm_count=152)
+        tiles, kb, slots = p["grid_m"] * p["grid_n"], p["k_iters"], p["ctas"] // 2
+        assert p["split_tiles"] == tiles and slots == min(76, cap * tiles), (M, N, K, p)
+        sched = check(tiles, kb, slots, True)
+        for whole, segs in sched:
+            assert whole == 0
+            for (_, _, _, role, f, l) in segs:
+                if role == OWNER:
+                    assert l - f + 1 <= cap - 1
