@@ -153,6 +153,10 @@ struct SplitK {
 };
 
 // planner.cu
+// Flops per byte of A, B and C; under kBandwidthBound the product is bandwidth-bound on
+// GB300 (the measured copy bandwidth and bf16 peak put the ridge near 280).
+constexpr double kBandwidthBound = 256.0;
+double intensity_of(const Problem &P);
 gemm_status_t check_args(const Problem &P);
 bool use_split_k(int stream_k, int64_t tiles, int64_t k_blocks, int64_t slots);
 gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan *out);

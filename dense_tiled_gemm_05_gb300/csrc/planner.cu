@@ -113,6 +113,13 @@ static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64
   return o;
 }
 
+double intensity_of(const Problem &P) {
+  const double es = esize_of(P.in_dtype), os = esize_of(P.out_dtype);
+  const double m = static_cast<double>(P.M), n = static_cast<double>(P.N),
+               k = static_cast<double>(P.K);
+  return 2.0 * m * n * k / (es * (m * k + k * n) + os * m * n);
+}
+
 // Tile slots of the CTA-pair kernel: one cluster of two SMs each, under the CTA cap.
 static int64_t pair_slots(int sm_count, int max_ctas) {
   int64_t clusters = sm_count > 1 ? sm_count / 2 : 1;
@@ -237,10 +244,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   pl.variant.esize = es;
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
-  // Flops per byte of A, B and C: under ~256 the product is bandwidth-bound on GB300.
-  const double intensity = 2.0 * P.M * P.N * P.K /
-                           (es * (static_cast<double>(P.M) * P.K + static_cast<double>(P.K) * P.N) +
-                            static_cast<double>(os) * P.M * P.N);
+  const double intensity = intensity_of(P);
   // CTA pairs (256-row tiles on two SMs) halve the shared-memory and L2 traffic per
   // flop; a problem no taller than one 128-row tile keeps single-CTA tiles, and so does a
   // compute-bound one whose 128 x 256 single-CTA tiles all run at once (one round on the
@@ -254,7 +258,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // 34.4 against 78.1; 128 x 128 x 65536: 61.8 against 289).
   const int64_t single_tiles = ((P.M + kTcBlockM - 1) / kTcBlockM) * ((P.N + 255) / 256);
   const int64_t narrow_kb = (P.K + 128 / es - 1) / (128 / es);
-  const bool one_round = single_tiles <= sm_count && intensity >= 256.0 && narrow_kb < 64;
+  const bool one_round = single_tiles <= sm_count && intensity >= kBandwidthBound && narrow_kb < 64;
   const bool few_tiles = opt.stream_k != 1 && narrow_kb >= 128 &&
                          2 * ((P.M + 255) / 256) * ((P.N + 127) / 128) <= pair_slots(sm_count, opt.max_ctas);
   pl.variant.pair = opt.cta_pair == 2 ||
@@ -288,7 +292,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
                           use_split_k(opt.stream_k, pair_tiles, narrow_kb, clusters);
   const bool wide_ok = pl.variant.pair && !chunked && es == 2 && !pl.a.mn_major && !pl.b.mn_major;
   if (opt.stage_k == 2 && !wide_ok) return GEMM_ERR_UNSUPPORTED;
-  pl.variant.kps = opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < 256.0 &&
+  pl.variant.kps = opt.stage_k == 2 || (opt.stage_k == 0 && wide_ok && intensity < kBandwidthBound &&
                                         opt.stream_k != 2 && !idle_split)
                        ? 2
                        : 1;

@@ -56,11 +56,8 @@ GEMM_API gemm_status_t gemm_tune(gemm_handle_t h, int64_t M, int64_t N, int64_t 
   if (pl0.info.path == GEMM_PATH_TCGEN05) {
     // Shorter pair tiles (96 rows per CTA) only for bandwidth-bound products (under ~256
     // flops per byte of A, B and C), where they can even out the rounds.
-    const int es = esize_of(in_dtype), os = esize_of(out_dtype);
-    const double intensity =
-        2.0 * M * N * K / (es * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
-                           static_cast<double>(os) * M * N);
-    const std::vector<int> rows_set = intensity < 256.0 ? std::vector<int>{0, 96} : std::vector<int>{0};
+    const std::vector<int> rows_set =
+        intensity_of(P) < kBandwidthBound ? std::vector<int>{0, 96} : std::vector<int>{0};
     for (int pair : {1, 2})
       for (int bn : {128, 256})
         for (int sk : {1, 2})
