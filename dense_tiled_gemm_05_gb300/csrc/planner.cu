@@ -251,11 +251,11 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   // SMs) with a short K-loop, where the pair's cross-SM handshakes cost more than they
   // save (bf16 2048^3: 17.1 against 19.0 us); from 64 K-blocks on, pairs win again (bf16
   // 2048^2 x 4096: 27.7 against 29.4 us; 2048^2 x 8192: 46.3 against 53.0). Bandwidth-bound
-  // ones keep pairs, for their wide stages. So do
-  // products with so few tiles that even 128-wide pair tiles leave more than half of the
-  // clusters idle, when K is long: the split-K rule then shares each tile's K-loop out
-  // (bf16 1024 x 512 x 8192: 27.5 against 41.3 us on single-CTA tiles; 512 x 1024 x 16384:
-  // 34.4 against 78.1; 128 x 128 x 65536: 61.8 against 289).
+  // ones keep pairs, for their wide stages. So do products with so few tiles that even
+  // 128-wide pair tiles leave more than half of the clusters idle, when K is long: the
+  // split-K rule then shares each tile's K-loop out (bf16 1024 x 512 x 8192: 27.5 against
+  // 41.3 us on single-CTA tiles; 512 x 1024 x 16384: 34.4 against 78.1; 128 x 128 x 65536:
+  // 61.8 against 289).
   const int64_t single_tiles = ((P.M + kTcBlockM - 1) / kTcBlockM) * ((P.N + 255) / 256);
   const int64_t narrow_kb = (P.K + 128 / es - 1) / (128 / es);
   const bool one_round = single_tiles <= sm_count && intensity >= kBandwidthBound && narrow_kb < 64;
@@ -265,8 +265,8 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
                     (opt.cta_pair == 0 && ((P.M > kTcBlockM && !one_round) || few_tiles));
   pl.variant.block_n =
       opt.block_n ? opt.block_n
-                  : pick_block_n(P.M, P.N, (P.K + 128 / es - 1) / (128 / es), pl.variant.pair,
-                                 split ? 1 : opt.stream_k, sm_count);
+                  : pick_block_n(P.M, P.N, narrow_kb, pl.variant.pair, split ? 1 : opt.stream_k,
+                                 sm_count);
   if (split || f16acc) {  // the chunked kernel has one shape: CTA pairs, 256 x 256 tiles
     pl.variant.exact = split;
     pl.variant.f16acc = f16acc;
@@ -274,17 +274,23 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
     pl.variant.block_n = 256;
   }
   const bool chunked = pl.variant.exact || pl.variant.f16acc;
+  // Rows of A per CTA of a pair tile (GEMM_OPT_TILE_ROWS; 128 by default). The MMA is
+  // always 128 rows per CTA; a CTA given fewer loads only those (the rest of its
+  // shared-memory rows feed accumulator lanes that are never stored). Shorter tiles do not
+  // pay by default: on bf16 M x 128 x 8192 the time stays that of one tile's K-loop, set by
+  // each SM's stream of A, whether 64 or 74 clusters run (M = 16384: 47.7 us with 256-row
+  // tiles, 50.5 us with 224), but two rounds of shorter tiles can beat one and a part
+  // (M = 24576: 71.8 us with 192-row tiles, 80.4 us with 256); gemm_tune tries them.
+  const bool rows_ok = pl.variant.pair && !chunked && !pl.a.mn_major;
+  if (opt.tile_rows && !rows_ok) return GEMM_ERR_UNSUPPORTED;
+  if (opt.tile_rows) pl.cta_rows = opt.tile_rows;
   // Two 128-byte K-blocks per stage (CTA-pair kernel, K-major 16-bit operands): each row
   // of A and B is then fetched 256 contiguous bytes at a time. By default only for
   // bandwidth-bound products (under ~256 flops per byte of A, B and C), where it measured
   // +1.5 % on bf16 16384 x 128 x 8192; compute-bound ones keep the deeper ring of one
-  // K-block per stage (4096^3 lost 9 % with wide stages). A forced split-K keeps narrow
-  // K-blocks, the finer unit it shares out (one 256 x 256 x 8192 tile: 128 units for 76
-  // clusters rather than 64).
-  // So does a product whose few tiles the split-K rule shares out over idle slots.
-  const bool rows_ok = pl.variant.pair && !chunked && !pl.a.mn_major;
-  if (opt.tile_rows && !rows_ok) return GEMM_ERR_UNSUPPORTED;
-  if (opt.tile_rows) pl.cta_rows = opt.tile_rows;
+  // K-block per stage (4096^3 lost 9 % with wide stages). A split-K keeps narrow K-blocks,
+  // the finer unit it shares out (one 256 x 256 x 8192 tile: 128 units for 76 clusters
+  // rather than 64): a forced one, and the one that shares few tiles out over idle slots.
   const int64_t clusters = pair_slots(sm_count, opt.max_ctas);
   const int64_t pair_tiles = ((P.M + 2 * pl.cta_rows - 1) / (2 * pl.cta_rows)) *
                              ((P.N + pl.variant.block_n - 1) / pl.variant.block_n);
@@ -296,14 +302,6 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
                                         opt.stream_k != 2 && !idle_split)
                        ? 2
                        : 1;
-  // Rows of A per CTA of a pair tile (GEMM_OPT_TILE_ROWS; 128 by default). The MMA is
-  // always 128 rows per CTA; a CTA given fewer loads only those (the rest of its
-  // shared-memory rows feed accumulator lanes that are never stored). Shorter tiles do not
-  // pay by default: on bf16 M x 128 x 8192 the time stays that of one tile's K-loop, set by
-  // each SM's stream of A, whether 64 or 74 clusters run (M = 16384: 47.7 us with 256-row
-  // tiles, 50.5 us with 224), but two rounds of shorter tiles can beat one and a part
-  // (M = 24576: 71.8 us with 192-row tiles, 80.4 us with 256); gemm_tune tries them.
-  // (Set above, before the stage width.)
   I.path = split ? GEMM_PATH_TCGEN05_3XTF32 : f16acc ? GEMM_PATH_TCGEN05_F16ACC : GEMM_PATH_TCGEN05;
   I.tile_m = pl.variant.pair ? 2 * pl.cta_rows : kTcBlockM;
   I.tile_n = pl.variant.block_n;
