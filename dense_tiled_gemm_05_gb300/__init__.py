@@ -45,7 +45,7 @@ EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_get_s
            "gemm_strerror", "gemm_set_option", "gemm_get_launch_count", "gemm_plan",
            "gemm_version", "gemm_run_noalloc", "gemm_schedule_segments", "gemm_run_host",
            "gemm_run_strided", "gemm_plan_strided", "gemm_tune", "gemm_tune_clear",
-           "gemm_softmax_rows")
+           "gemm_softmax_rows", "gemm_set_kernel_events")
 
 
 class GemmError(RuntimeError):
@@ -138,6 +138,8 @@ def lib():
                 L.gemm_set_option.restype = i32
                 L.gemm_get_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
                 L.gemm_get_launch_count.restype = i32
+                L.gemm_set_kernel_events.argtypes = [vp, vp, vp]
+                L.gemm_set_kernel_events.restype = i32
                 L.gemm_plan.argtypes = run_args + [i32, i32, ctypes.c_int32,
                                                    ctypes.POINTER(PlanInfo)]
                 L.gemm_plan.restype = i32
@@ -219,6 +221,19 @@ class Gemm:
         n = ctypes.c_uint64()
         _check(lib().gemm_get_launch_count(self._h, ctypes.byref(n)))
         return n.value
+
+    def set_kernel_events(self, start=None, end=None):
+        """Record two torch.cuda.Event objects around the main GEMM kernel of every later
+        product on this handle (after any staging copies); no arguments turn it off. The
+        events must have been recorded once, so that their CUDA events exist."""
+        if start is None or end is None:
+            _check(lib().gemm_set_kernel_events(self._h, None, None), "gemm_set_kernel_events")
+            self._kernel_events = None
+            return
+        self._kernel_events = (start, end)  # kept alive while the hook is set
+        _check(lib().gemm_set_kernel_events(self._h, ctypes.c_void_p(start.cuda_event),
+                                            ctypes.c_void_p(end.cuda_event)),
+               "gemm_set_kernel_events")
 
     def status(self, stream=None):
         """Synchronise the stream and return the device status code (0 = OK), cleared."""

@@ -56,6 +56,8 @@ struct gemm_handle_s {
   cudaEvent_t hp_event[2 + 4 * kMaxPanels] = {};
   bool hp_ready = false;
   std::vector<TuneEntry> tuned;  // gemm_tune's choices, by problem signature
+  // gemm_set_kernel_events: caller's events recorded around the main kernel's launch
+  cudaEvent_t kernel_events[2] = {nullptr, nullptr};
 };
 
 namespace gemm_gb300 {
@@ -171,7 +173,10 @@ cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t 
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
                         const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,
                         int group_m, int debug_flags, SplitK sk, cudaStream_t s);
-gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s);
+// record_events: record the handle's gemm_set_kernel_events pair around the main kernel
+// (the calls gemm_set_kernel_events documents; not the host pipeline or the tuner).
+gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s,
+                      bool record_events = true);
 
 }  // namespace api
 }  // namespace gemm_gb300

@@ -167,6 +167,14 @@ GEMM_API gemm_status_t gemm_get_launch_count(gemm_handle_t h, uint64_t *count) {
   return GEMM_OK;
 }
 
+GEMM_API gemm_status_t gemm_set_kernel_events(gemm_handle_t h, void *start_event,
+                                              void *end_event) {
+  if (!h || (start_event == nullptr) != (end_event == nullptr)) return GEMM_ERR_INVALID_ARG;
+  h->kernel_events[0] = static_cast<cudaEvent_t>(start_event);
+  h->kernel_events[1] = static_cast<cudaEvent_t>(end_event);
+  return GEMM_OK;
+}
+
 GEMM_API gemm_status_t gemm_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
                                  int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc,
                                  gemm_dtype_t in_dtype, gemm_dtype_t out_dtype,

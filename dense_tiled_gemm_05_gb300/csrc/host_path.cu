@@ -158,7 +158,7 @@ GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int6
     Plan pl;
     st = make_plan(P, options_for(h, P), h->sm_count, &pl);
     if (st != GEMM_OK) return st;
-    st = execute(h, P, pl, s_mm);
+    st = execute(h, P, pl, s_mm, false);
     if (st != GEMM_OK) return st;
     if ((e = cudaEventRecord(e_mm[step], s_mm)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(s_out, e_mm[step], 0)) != cudaSuccess ||

@@ -240,9 +240,12 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "tcgen05 launch");
 }
 
-gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s) {
+gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s,
+                      bool record_events) {
   const gemm_plan_info_t &I = pl.info;
   cudaError_t e;
+  const cudaEvent_t ev0 = record_events ? h->kernel_events[0] : nullptr;
+  const cudaEvent_t ev1 = record_events ? h->kernel_events[1] : nullptr;
   switch (I.path) {
     case GEMM_PATH_NONE: return GEMM_OK;
     case GEMM_PATH_ZERO_FILL:
@@ -253,9 +256,13 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
     case GEMM_PATH_FMA: {
       FmaParams fp{P.M, P.N, P.K, P.A, P.lda, P.B, P.ldb, P.C, P.ldc, P.in_dtype, P.out_dtype,
                    P.a_layout == GEMM_COL_MAJOR, P.b_layout == GEMM_COL_MAJOR, pl.acc_chunk};
+      if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess)
+        return cuda_fail(e, "record the kernel start event");
       e = fma_launch(fp, pl.fma_tile, s);
       if (e != cudaSuccess) return cuda_fail(e, "fma launch");
       h->launches += 1;
+      if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess)
+        return cuda_fail(e, "record the kernel end event");
       return GEMM_OK;
     }
     default: break;
@@ -282,10 +289,14 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   SplitK sk;
   sk.h = h;
   sk.mode = pl.stream_k;
+  if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess)
+    return cuda_fail(e, "record the kernel start event");
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
                  pl.group_m, h->stall_producer ? kDebugStallProducer : 0, sk, s);
   if (st != GEMM_OK) return st;
   h->launches += 1;
+  if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess)
+    return cuda_fail(e, "record the kernel end event");
   return GEMM_OK;
 }
 

@@ -15,8 +15,9 @@ using namespace gemm_gb300::api;
 // memory pool), deployments that reserve all device memory up front and forbid growth,
 // and host callbacks or real-time paths where a cudaMalloc (which may synchronise the
 // device) is not allowed. gemm_run_noalloc serves them without a handle: the staging
-// copies that misaligned operands and MN-major tf32 operands need go to a fixed, file-scope
-// device array instead of a workspace that grows on demand.
+// copies that misaligned operands and MN-major tf32 operands need, and the tf32 hi/lo
+// split operands of exact fp32, go to a fixed, file-scope device array instead of a
+// workspace that grows on demand.
 namespace {
 
 constexpr size_t kStaticStatusBytes = 256;  // first 256 bytes: the call's status word
@@ -79,7 +80,8 @@ gemm_status_t execute_noalloc(void *scratch, int *status, const Problem &P, cons
   const size_t limit = GEMM_NOALLOC_SCRATCH_BYTES - kStaticStatusBytes;
   if (static_cast<size_t>(I.workspace_bytes) > limit) {
     if (log_enabled())
-      std::fprintf(stderr, "[gemm] gemm_run_noalloc: staging needs %lld bytes, limit %zu\n",
+      std::fprintf(stderr, "[gemm] gemm_run_noalloc: %s needs %lld bytes of scratch, limit %zu\n",
+                   I.path == GEMM_PATH_TCGEN05_3XTF32 ? "exact fp32 (split operands)" : "staging",
                    static_cast<long long>(I.workspace_bytes), limit);
     return GEMM_ERR_UNSUPPORTED;
   }
@@ -136,13 +138,7 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(
   whole.stream_k = 1;
   st = make_plan(P, whole, sms, &pl);
   if (st != GEMM_OK) return st;
-  if (pl.info.path == GEMM_PATH_TCGEN05_3XTF32 &&
-      static_cast<size_t>(pl.info.workspace_bytes) > GEMM_NOALLOC_SCRATCH_BYTES - kStaticStatusBytes) {
-    // Exact fp32 whose split operands do not fit the array: the fp32 FMA kernel needs none.
-    Options fma = whole;
-    fma.force_path = 2;
-    st = make_plan(P, fma, sms, &pl);
-    if (st != GEMM_OK) return st;
-  }
+  // Staged copies and the split hi/lo operands of exact fp32 alike must fit the array;
+  // a problem that needs more is refused (execute_noalloc) before anything is launched.
   return execute_noalloc(scratch, device_status, P, pl, static_cast<cudaStream_t>(cuda_stream));
 }

@@ -91,10 +91,10 @@ GEMM_API gemm_status_t gemm_tune(gemm_handle_t h, int64_t M, int64_t N, int64_t 
   float best = 0.0f, first = 0.0f;
   size_t best_i = 0;
   for (size_t i = 0; i < cands.size() && st == GEMM_OK; ++i) {
-    st = execute(h, P, cands[i].pl, s);  // warm-up: workspaces sized, code loaded
+    st = execute(h, P, cands[i].pl, s, false);  // warm-up: workspaces sized, code loaded
     for (int r = 0; r < iters && st == GEMM_OK; ++r) {
       if (r == 0 && cudaEventRecord(e0, s) != cudaSuccess) st = GEMM_ERR_CUDA;
-      if (st == GEMM_OK) st = execute(h, P, cands[i].pl, s);
+      if (st == GEMM_OK) st = execute(h, P, cands[i].pl, s, false);
     }
     float ms = 0.0f;
     if (st == GEMM_OK && (cudaEventRecord(e1, s) != cudaSuccess ||

@@ -124,8 +124,11 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
 
 /* C = A @ B with explicit operand layouts, enqueued on `cuda_stream` (a
  * cudaStream_t; NULL = legacy default stream). The host-side planner picks the
- * kernel (tcgen05 tensor-core path for 16-bit inputs and tf32 mode, fp32 FMA
- * path for exact mode), stages misaligned operands, and launches.
+ * kernel -- the tcgen05 tensor-core kernels for 16-bit inputs and tf32 mode; for exact
+ * fp32, the tensor cores on operands split once into tf32 hi and lo parts (three tf32
+ * products, K summed in 128-long chunks in fp32 registers), or the fp32 FMA kernel for
+ * problems too small to fill the tensor-core tiles -- stages misaligned operands, and
+ * launches.
  * Errors (nothing launched): INVALID_ARG for h == NULL, negative sizes, a null
  * pointer with a non-empty extent, a leading dimension below its minimum, an
  * unknown enum, or C's span overlapping A's or B's; UNSUPPORTED for a
@@ -205,6 +208,18 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
 
 /* Number of kernels this handle has launched since it was created. */
 GEMM_API gemm_status_t gemm_get_launch_count(gemm_handle_t h, uint64_t *count);
+
+/* Timing hook for the main kernel of a product. With start_event and end_event both
+ * cudaEvent_t handles (created by the caller, on this handle's device), every later
+ * gemm_run / gemm_run_ex / gemm_run_strided call on this handle records start_event on
+ * its stream immediately before it launches the GEMM kernel itself -- after any staging
+ * copies (misaligned operands, transposed tf32 operands, the hi/lo split of exact fp32)
+ * -- and end_event immediately after it, so that the caller can time that kernel apart
+ * from the copies with cudaEventElapsedTime. Both NULL turns the hook off (the default).
+ * The events stay owned by the caller, who must keep them alive while the hook is set.
+ * Errors: INVALID_ARG for h == NULL or exactly one of the two events NULL. */
+GEMM_API gemm_status_t gemm_set_kernel_events(gemm_handle_t h, void *start_event,
+                                              void *end_event);
 
 /* ------------------------------------------------------------- planning */
 
@@ -380,11 +395,16 @@ GEMM_API const char *gemm_version(void);
  * library routine. Operands that must be staged (a base or leading dimension TMA cannot
  * address, or an MN-major fp32 operand in tf32 mode) are copied into a file-scope device
  * array of GEMM_NOALLOC_SCRATCH_BYTES that every GPU loading this library keeps until the
- * process exits. A call whose staged copies would not fit returns GEMM_ERR_UNSUPPORTED
- * before launching anything; use gemm_run_ex for it. Arguments and layouts are those of
- * gemm_run_ex; the device is the caller's current device; default options apply, except
- * that tiles are never split along K (GEMM_OPT_STREAM_K = 1: split-K's partial tiles
- * live in a handle's workspace).
+ * process exits. Exact fp32 (GEMM_PREC_EXACT_FP32, or DEFAULT with fp32 inputs) also uses
+ * that array: beyond the smallest problems (which run on the FMA kernel and need nothing)
+ * both operands are split into tf32 hi and lo parts there, about
+ * 8 * (M + N) * round_up(K, 32) bytes. A call whose staged copies or split operands would
+ * not fit in GEMM_NOALLOC_SCRATCH_BYTES - 256 bytes returns GEMM_ERR_UNSUPPORTED before
+ * launching anything (it never falls back to a slower kernel); use gemm_run_ex for it
+ * (with GEMM_OPT_FORCE_PATH = 2 for the FMA kernel, which needs no scratch). Arguments
+ * and layouts are those of gemm_run_ex; the device is the caller's current device;
+ * default options apply, except that tiles are never split along K
+ * (GEMM_OPT_STREAM_K = 1: split-K's partial tiles live in a handle's workspace).
  *
  * The first call on each device does a one-time set-up with that device current (it looks
  * up the array's device address and the SM count); make that first call before any

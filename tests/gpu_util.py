@@ -57,12 +57,15 @@ def rel_err(c_gpu, C64, D):
     return float(np.max(np.abs(c[~zero] - C64[~zero]) / D[~zero]))
 
 
-def sample_rows(M, tile=128, n_random=32, seed=0):
-    """Every tile's first and last row for every other tile-row, plus random rows."""
+def sample_rows(M, tile=256, n_random=256, seed=0):
+    """Rows i = 0, 127, 128 and 255 mod 256 of every 256-row tile-row (the first and last
+    rows of both CTAs of a pair tile, and of every 128-row single-CTA tile), the last row,
+    plus n_random random rows."""
     rows = set()
-    for t0 in range(0, M, 2 * tile):
-        rows.add(t0)
-        rows.add(min(t0 + tile - 1, M - 1))
+    for t0 in range(0, M, tile):
+        for r in (0, tile // 2 - 1, tile // 2, tile - 1):
+            if t0 + r < M:
+                rows.add(t0 + r)
     rows.add(M - 1)
     rng = np.random.default_rng(seed)
     rows.update(rng.integers(0, M, n_random).tolist())
@@ -73,6 +76,12 @@ def check_sampled(p, c_gpu, rows=None):
     rows = sample_rows(p.M) if rows is None else rows
     C64, D = oracle_rows(p, rows)
     return rel_err(c_gpu[rows], C64, D)
+
+
+def check_full(p, c_gpu, oracle_result=None):
+    """Every element of C against the oracle's full product (computed here unless given)."""
+    C64, D = oracle_rows(p) if oracle_result is None else oracle_result
+    return rel_err(c_gpu, C64, D)
 
 
 def check_sums(p, c_gpu):

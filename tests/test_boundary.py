@@ -58,6 +58,7 @@ def test_null_handle_is_rejected(L):
     assert L.gemm_tune(None, 4, 4, 4, None, 4, None, 4, None, 4, 0, 0, 0, 0, 0, None, 1,
                        None) == 1
     assert L.gemm_tune_clear(None) == 1
+    assert L.gemm_set_kernel_events(None, None, None) == 1
     assert L.gemm_set_option(None, 0, 1) == 1
     L.gemm_destroy(None)  # no-op
 

@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_util import (check_sampled, check_sums, oracle_rows, rel_err, run_gpu, sample_rows,
-                      to_device, tolerance)
+from gpu_util import (check_full, check_sampled, check_sums, oracle_rows, rel_err, run_gpu,
+                      sample_rows, to_device, tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -342,14 +342,34 @@ def test_deterministic(h):
 
 
 # ------------------------------------------------------- full-size configs
+#
+# Every element of every full-size product is compared with the oracle's fp64 product
+# (the whole 8192^3 takes about 15 s on the host's cores), plus every row and column sum.
+
+_ORACLE = {}
+
+
+def oracle_full(p):
+    """The oracle's full (C, D) for a workload; fp32 inputs shared by both precision modes
+    are computed once."""
+    key = (p.name.replace("_tf32", "").replace("_exact", ""), p.M, p.N, p.K)
+    if key not in _ORACLE:
+        _ORACLE.clear()  # one full-size result held at a time (8192^2 fp64 is 1 GB)
+        _ORACLE[key] = oracle_rows(p)
+    return _ORACLE[key]
+
+
+def full_size_check(p, c):
+    err = check_full(p, c, oracle_full(p))
+    assert err <= tolerance(p), "%s: rel err %.3g > %.3g" % (p.name, err, tolerance(p))
+    s_err, tol = check_sums(p, c)
+    assert s_err <= tol, s_err
+    return err
+
 
 def test_bf16_4096_col_major_b(h):
     p = W.bf16_square(4096)
-    c = run_gpu(h, p)
-    err = check_sampled(p, c)
-    assert err <= tolerance(p), err
-    s_err, tol = check_sums(p, c)
-    assert s_err <= tol, s_err
+    full_size_check(p, run_gpu(h, p))
 
 
 @pytest.mark.parametrize("precision,force_path", [("tf32", 0), ("exact", 0), ("exact", 2)],
@@ -361,28 +381,20 @@ def test_fp32_4096_modes(h, precision, force_path):
     h2.set_option("force_path", force_path)
     c = run_gpu(h2, p)
     h2.close()
-    err = check_sampled(p, c)
-    assert err <= tolerance(p), (precision, err)
-    s_err, tol = check_sums(p, c)
-    assert s_err <= tol, s_err
+    full_size_check(p, c)
 
 
 def test_bf16_8192(h):
     p = W.bf16_square(8192, seed=5)
     c = run_gpu(h, p)
-    err = check_sampled(p, c, rows=None)
-    assert err <= tolerance(p), err
-    s_err, tol = check_sums(p, c)
-    assert s_err <= tol, s_err
+    full_size_check(p, c)
+    # the tile-boundary rows (0, 127, 128, 255 mod 256) once more through the row sampler
+    assert check_sampled(p, c) <= tolerance(p)
 
 
 def test_bf16_skinny(h):
     p = W.bf16_skinny()
-    c = run_gpu(h, p)
-    err = check_sampled(p, c)
-    assert err <= tolerance(p), err
-    s_err, tol = check_sums(p, c)
-    assert s_err <= tol, s_err
+    full_size_check(p, run_gpu(h, p))
 
 
 @pytest.mark.parametrize("block_n", [128, 256])

@@ -46,20 +46,26 @@ def test_noalloc_matches_run_ex_on_calls_in_a_row(g):
     # The allocation-free path computes whole tiles only (no split-K workspace); compare
     # with the handle path on the same schedule so the bits must agree.
     h.set_option("stream_k", 1)
-    # Both need staging: fp16 rows of 1025 elements are not 16-byte multiples, and a
-    # row-major B in tf32 mode is transposed into K-major form.
-    problems = [W.ragged(1023, 1000, 1025), W.fp32_square(1000, "tf32", seed=21),
-                W.ragged(1023, 1000, 1025)]
+    # All need scratch: fp16 rows of 1025 elements are not 16-byte multiples, a row-major B
+    # in tf32 mode is transposed into K-major form, and exact fp32 splits both operands
+    # into tf32 hi and lo parts. The tf32 problem runs twice: once with the array's own
+    # status word, once with the caller's, so a timeout on that kernel would be seen.
+    problems = [(W.ragged(1023, 1000, 1025), True), (W.fp32_square(1000, "tf32", seed=21), False),
+                (W.fp32_square(1000, "tf32", seed=21), True),
+                (W.ragged(1000, 700, 1025, seed=22, dtype="f32"), True),
+                (W.ragged(1023, 1000, 1025), True)]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for n, p in enumerate(problems):
+    for p, own_status in problems:
         a, b = to_device(p.A), to_device(p.B)
-        plan = g.plan(a, b, out_dtype=p.out_dtype, precision=p.precision)
+        plan = h.plan(a, b, out_dtype=p.out_dtype, precision=p.precision)
         assert plan["stage_a"] or plan["stage_b"]
         assert plan["workspace_bytes"] <= (32 << 20) - 256  # fits the fixed array
+        if p.precision == "exact":
+            assert plan["path"] == "tcgen05_3xtf32", plan  # split operands in the array
         ref = h.matmul(a, b, out_dtype=p.out_dtype, precision=p.precision)  # gemm_run_ex
         assert h.status() == 0
         out = torch.full_like(ref, float("nan"))
-        rc = noalloc(g, a, b, out, p.precision, status=status if n != 1 else None)
+        rc = noalloc(g, a, b, out, p.precision, status=status if own_status else None)
         assert rc == 0, g.STATUS.get(rc, rc)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
@@ -81,3 +87,23 @@ def test_noalloc_rejects_staging_beyond_its_array(g):
     assert rc == 2  # GEMM_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert bool((out == 7.0).all())
+
+
+def test_noalloc_rejects_exact_split_beyond_its_array(g):
+    # Exact fp32 2048^3 splits both operands into hi and lo parts: 8 * 4096 * 2048 bytes =
+    # 64 MiB, more than the array holds. Refused (no silent fall-back to a slower kernel),
+    # C untouched; the same problem through the handle path is correct.
+    p = W.ragged(2048, 2048, 2048, seed=23, dtype="f32")
+    a, b = to_device(p.A), to_device(p.B)
+    out = torch.full((2048, 2048), 7.0, dtype=torch.float32, device="cuda")
+    rc = noalloc(g, a, b, out, "exact")
+    assert rc == 2  # GEMM_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+    h = g.Gemm(0)
+    c = h.matmul(a, b, precision="exact")
+    assert h.status() == 0
+    h.close()
+    rows = list(range(0, 2048, 61)) + [2047]
+    C64, D = oracle_rows(p, rows)
+    assert rel_err(c[rows], C64, D) <= tolerance(p)
