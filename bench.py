@@ -647,6 +647,17 @@ def timed_steps(h, step, n, stream, dev, period_ms=200, dist=None, events=True):
     return t0.elapsed_time(t1), step_ms, kernel_ms, launches, clocks.summary()
 
 
+def kernel_duration(region_ms, steps, launches, kernel_ms_mean):
+    """The dominant kernel's average duration for the roofline, and how it was taken. When
+    every step is that one kernel (no staging copies), the timed region's events divided by
+    the launches: back to back, each launch's prologue overlaps the previous launch's tail,
+    which events recorded between launches would prevent. Otherwise the mean of the events
+    the library records around that kernel alone."""
+    if launches == steps:
+        return region_ms / steps, "timed region / launches (one kernel per step, back to back)"
+    return kernel_ms_mean, "events around the kernel alone (after its staging copies), mean"
+
+
 def roofline(p, bound, workload_name, kernel_ms, peaks, peak_src, sustained_peak):
     """Roofline of the dominant kernel: algorithmic flops (or bytes) per launch over its
     mean event-timed duration, against the measured peak for its dtype and bound."""
@@ -717,6 +728,11 @@ def measure_config(g, dev, name, peaks, peak_src, min_s=0.3, cpu_s=3.0):
     kname, plan = kernel_name(h, sets[0][0], sets[0][1], p)
     kp = percentiles(kern_ms)
     flops = 2.0 * p.M * p.N * p.K
+    k_ms, k_how = kernel_duration(elapsed_ms, n, launches, kp["mean"])
+    roof = roofline(p, bound, name, k_ms, peaks, peak_src, False)
+    roof["kernel_ms"], roof["kernel_ms_from"] = k_ms, k_how
+    roof["frac_event_bracketed"] = roofline(p, bound, name, kp["mean"], peaks, peak_src,
+                                            False)["frac"]
     out = {"workload": desc, "value": flops * n / (elapsed_ms / 1e3) / 1e12, "unit": "TFLOP/s",
            "steps": n, "ms_per_step": elapsed_ms / n, "step_ms": percentiles(step_ms),
            "kernel": kname, "kernel_ms": kp,
@@ -724,7 +740,7 @@ def measure_config(g, dev, name, peaks, peak_src, min_s=0.3, cpu_s=3.0):
            "staging_launches_per_step": (launches - n) / n,
            "plan": {k: plan[k] for k in ("path", "tile_m", "tile_n", "ctas", "split_tiles",
                                          "stage_a", "stage_b")},
-           "roofline": roofline(p, bound, name, kp["mean"], peaks, peak_src, False),
+           "roofline": roof,
            "clocks": clocks, "gpu_launches": launches,
            "l2": "inputs larger than L2: %d buffer sets rotated" % len(sets),
            "dtype": {"bf16": "bf16", "f32": "tf32" if p.precision == "tf32" else "f32"}[p.in_dtype]}
@@ -843,8 +859,12 @@ def main():
     # A region of a second or more runs under the power cap: the sustained cuBLAS figure
     # is its denominator; shorter regions use the burst figure.
     long_run = elapsed_ms >= 1000.0
-    roof = roofline(p, bound, args.workload, kp["mean"], peaks, peak_src, long_run)
+    k_ms, k_how = kernel_duration(elapsed_ms, args.steps, launches, kp["mean"])
+    roof = roofline(p, bound, args.workload, k_ms, peaks, peak_src, long_run)
     roof["peak_source"] += "; timed region %.3f s" % (elapsed_ms / 1e3)
+    roof["kernel_ms"], roof["kernel_ms_from"] = k_ms, k_how
+    roof["frac_event_bracketed"] = roofline(p, bound, args.workload, kp["mean"], peaks,
+                                            peak_src, long_run)["frac"]
 
     # The same product back to back for seconds, whatever --steps is: the steady state
     # under the power cap, with a 50 ms clock record.
@@ -858,6 +878,8 @@ def main():
         s_ms = max_over_ranks(s_ms, dist, dev)
         skp = percentiles(s_kern)
         s_roof = roofline(p, bound, args.workload, skp["mean"], peaks, peak_src, True)
+        s_roof["kernel_ms"] = skp["mean"]
+        s_roof["kernel_ms_from"] = "events around each kernel, mean"
         sustained = {"steps": n, "seconds": s_ms / 1e3,
                      "value": job_rate(flops * n, world, s_ms) / 1e12, "unit": "TFLOP/s",
                      "ms_per_step": s_ms / n, "step_ms": percentiles(s_step), "kernel_ms": skp,

@@ -33,7 +33,7 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
 OPTIONS = {"wait_timeout_us": 0, "force_path": 1, "group_m": 2, "max_ctas": 3,
            "fault_stall_producer": 4, "force_staging": 5, "cta_pair": 6,
            "block_n": 7, "exact_chunk": 8, "stream_k": 9, "host_panel": 10, "acc_chunk": 11, "stage_k": 12,
-           "tile_rows": 13}
+           "tile_rows": 13, "tf32_transpose": 14}
 PATHS = {0: "none", 1: "zero_fill", 2: "tcgen05", 3: "fma", 4: "tcgen05_3xtf32",
          5: "tcgen05_f16acc"}
 _DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}

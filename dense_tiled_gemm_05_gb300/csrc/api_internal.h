@@ -41,6 +41,7 @@ struct gemm_handle_s {
   int stage_k = 0;      // 128-byte K-blocks per stage of the CTA-pair kernel, 0 auto
   int tile_rows = 0;    // rows of A per CTA of the CTA-pair kernel, 0 auto
   int stream_k = 0;     // 0 auto (on), 1 off
+  int tf32_transpose = 0;  // 1: MN-major tf32 operands staged transposed (K-major)
   int host_panel = 0;  // gemm_run_host panel width (rows of A, columns of B), 0 auto
   // split-K workspace of the CTA-pair kernel: partial tiles and flags
   void *sk_ws = nullptr;
@@ -110,6 +111,7 @@ struct Problem {
 struct Options {
   int force_path = 0, group_m = 8, max_ctas = 0, force_staging = 0, cta_pair = 0, block_n = 0;
   int stream_k = 0, exact_chunk = 0, acc_chunk = 0, stage_k = 0, tile_rows = 0;
+  int tf32_transpose = 0;
 };
 
 // fp16-accumulator chunk (K elements per fp16 rounding of the running total) when the
@@ -120,8 +122,8 @@ constexpr int kDefaultAccChunk = 16;
 // elements with leading dimension ld (in elements). It is either read in place or staged
 // into the workspace first: copied when TMA cannot address it (misaligned base or
 // leading dimension), transposed into K-major form when it is an MN-major operand of a
-// kernel that reads K-major operands only (tf32, which the tensor cores take K-major only
-// on GB300, and the fp16-accumulator kernel), or split into tf32
+// kernel that reads K-major operands only (the fp16-accumulator kernel) or a tf32 operand
+// under GEMM_OPT_TF32_TRANSPOSE, or split into tf32
 // hi/lo parts (exact-fp32 mode; always K-major: [hi | lo], each part K columns
 // zero-padded to split_kp, a whole number of 32-long K-blocks).
 struct OperandPlan {
@@ -168,7 +170,7 @@ Options options_for(gemm_handle_t h, const Problem &P);
 
 // launch.cu
 bool encode_2d(CUtensorMap *m, int dtype, const void *base, int64_t inner, int64_t outer,
-               int64_t ld, uint32_t box_inner, uint32_t box_outer);
+               int64_t ld, uint32_t box_inner, uint32_t box_outer, bool atom32 = false);
 cudaError_t stage_operand(const OperandPlan &o, void *dst, int es, cudaStream_t s);
 gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int64_t a_ld,
                         const void *b_ptr, int64_t b_ld, int *status, uint64_t timeout_ns,

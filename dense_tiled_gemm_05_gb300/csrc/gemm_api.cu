@@ -129,6 +129,10 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->cta_pair = static_cast<int>(v);
       return GEMM_OK;
+    case GEMM_OPT_TF32_TRANSPOSE:
+      if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
+      h->tf32_transpose = static_cast<int>(v);
+      return GEMM_OK;
     case GEMM_OPT_STAGE_K:
       if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
       h->stage_k = static_cast<int>(v);

@@ -57,9 +57,10 @@ static CUtensorMapDataType tmap_dtype(int dt) {
 }
 
 // 2D tensor map: dims {inner, outer}, row pitch ld elements, box {box_inner, box_outer},
-// 128-byte swizzle, zero fill outside the tensor.
+// 128-byte swizzle (of 16-byte chunks, or of 32-byte atoms with atom32, the form the
+// tensor cores read an MN-major tf32 operand in), zero fill outside the tensor.
 bool encode_2d(CUtensorMap *m, int dtype, const void *base, int64_t inner, int64_t outer,
-               int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+               int64_t ld, uint32_t box_inner, uint32_t box_outer, bool atom32) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int es = esize_of(dtype);
@@ -70,7 +71,8 @@ bool encode_2d(CUtensorMap *m, int dtype, const void *base, int64_t inner, int64
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, tmap_dtype(dtype), 2, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  atom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS && log_enabled())
     std::fprintf(stderr, "[gemm] cuTensorMapEncodeTiled failed (%d)\n", static_cast<int>(r));
@@ -158,9 +160,9 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   const uint32_t a_box_outer = pl.a.mn_major ? row_elems : cta_rows_a;
   const uint32_t b_box_outer = pl.b.mn_major ? row_elems : cta_rows_b;
   if (!encode_2d(&tmA, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, row_elems,
-                 a_box_outer) ||
+                 a_box_outer, es == 4 && pl.a.mn_major) ||
       !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
-                 b_box_outer))
+                 b_box_outer, es == 4 && pl.b.mn_major))
     return GEMM_ERR_CUDA;
   if (I.tma_store) {
     const uint32_t out_row = 128 / esize_of(P.out_dtype);

@@ -77,6 +77,8 @@ static bool tma_legal(const void *p, int64_t ld, int64_t outer, int es) {
 static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64_t ld, int layout,
                                 bool k_is_rows_dim, int es, bool force_stage, bool split_hl,
                                 bool k_major_only, size_t *ws_cursor) {
+  // (k_major_only: the kernel reads this operand K-major only, so an MN-major one is
+  // staged transposed)
   OperandPlan o{};
   o.ptr = p;
   o.ld = ld;
@@ -92,7 +94,7 @@ static OperandPlan plan_operand(const void *p, int64_t rows, int64_t cols, int64
   o.k_outer = o.outer;
   o.k_inner = o.inner;
   o.split_hl = split_hl;
-  o.transpose = !split_hl && o.mn_major && (es == 4 || k_major_only);
+  o.transpose = !split_hl && o.mn_major && k_major_only;
   o.staged = split_hl || o.transpose || force_stage || !tma_legal(p, ld, o.outer, es);
   if (o.staged) {
     if (split_hl) {
@@ -237,10 +239,13 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   const int es = esize_of(P.in_dtype);
   const int os = esize_of(P.out_dtype);
   size_t cursor = 0;
+  // K-major only: the fp16-accumulator kernel; tf32 operands when the option asks for the
+  // transposed copy (by default the tensor cores read MN-major tf32 in place).
+  const bool k_major_only = f16acc || (es == 4 && opt.tf32_transpose != 0);
   pl.a = plan_operand(P.A, P.M, P.K, P.lda, P.a_layout, false, es, opt.force_staging != 0, split,
-                      f16acc, &cursor);
+                      k_major_only, &cursor);
   pl.b = plan_operand(P.B, P.K, P.N, P.ldb, P.b_layout, true, es, opt.force_staging != 0, split,
-                      f16acc, &cursor);
+                      k_major_only, &cursor);
   pl.variant.esize = es;
   pl.variant.a_mn = pl.a.mn_major;
   pl.variant.b_mn = pl.b.mn_major;
@@ -368,6 +373,7 @@ Options options_of(gemm_handle_t h) {
     o.acc_chunk = h->acc_chunk;
     o.stage_k = h->stage_k;
     o.tile_rows = h->tile_rows;
+    o.tf32_transpose = h->tf32_transpose;
   }
   return o;
 }

@@ -243,14 +243,32 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // in bits 32-45, descriptor version 1 in bits 46-47, base offset 0 (tiles are 1024-byte
 // aligned), swizzle mode 2 (128B) in bits 61-63.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
+                                                uint32_t sbo_bytes, uint32_t mode = 2) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(mode & 7u) << 61;
   return d;
+}
+
+// Swizzle mode of an operand's shared-memory descriptor: 128-byte rows with 16-byte
+// chunks swizzled (mode 2) for every K-major operand and for MN-major 16-bit ones; an
+// MN-major tf32 operand is read in the 128-byte swizzle with 32-byte atoms (mode 1), the
+// layout a TMA load with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B writes.
+template <int ESIZE, bool MN>
+__device__ __forceinline__ constexpr uint32_t sdesc_mode() {
+  return (MN && ESIZE == 4) ? 1u : 2u;
+}
+
+// Stride-dimension byte offset of an MN-major operand stored as 128-byte rows, one row
+// per K index: the distance between the groups of K rows one swizzle atom holds -- eight
+// rows (1024 bytes) in the 16-byte-chunk swizzle, four (512 bytes) in the 32-byte-atom
+// swizzle of tf32.
+template <int ESIZE>
+__device__ __forceinline__ constexpr uint32_t sdesc_mn_sbo() {
+  return ESIZE == 4 ? 512u : 1024u;
 }
 
 // ------------------------------------------------------------- CTA pairs (2-SM)

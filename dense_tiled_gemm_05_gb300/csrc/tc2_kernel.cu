@@ -218,10 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a_k = (kk / G::BOX_STEPS) * G::A_BOX_BYTES + (kk % G::BOX_STEPS) * 32;
             const uint32_t b_k = (kk / G::BOX_STEPS) * G::B_BOX_BYTES + (kk % G::BOX_STEPS) * 32;
             const uint64_t ad =
-                A_MN ? sdesc_sw128(a_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
+                A_MN ? sdesc_sw128(a_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES,
+                                  sdesc_mn_sbo<ESIZE>(), sdesc_mode<ESIZE, true>())
                      : sdesc_sw128(a_base + a_k, 16, 1024);
             const uint64_t bd =
-                B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
+                B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES,
+                                  sdesc_mn_sbo<ESIZE>(), sdesc_mode<ESIZE, true>())
                      : sdesc_sw128(b_base + b_k, 16, 1024);
             const uint32_t accumulate = (kb != seg.kb_begin) || kk != 0;
             if (ESIZE == 2)
@@ -449,7 +451,6 @@ int tc2_max_active_clusters() {
 cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const CUtensorMap &tmC, const CUtensorMap &tmP, const TcParams &p, int grid,
                        cudaStream_t s) {
-  // tf32 operands are always K-major (MN-major fp32 operands are staged transposed).
   if (v.kps == 2 && v.esize == 2 && !v.a_mn && !v.b_mn) {
     if (v.block_n == 256) return launch_pair<2, false, false, 256, 2>(tmA, tmB, tmC, tmP, p, grid, s);
     if (v.block_n == 128) return launch_pair<2, false, false, 128, 2>(tmA, tmB, tmC, tmP, p, grid, s);
@@ -459,10 +460,10 @@ cudaError_t tc2_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtenso
     return launch_pair_majors<2, 256>(v, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.esize == 2 && v.block_n == 128)
     return launch_pair_majors<2, 128>(v, tmA, tmB, tmC, tmP, p, grid, s);
-  if (v.esize == 4 && !v.a_mn && !v.b_mn) {
-    if (v.block_n == 256) return launch_pair<4, false, false, 256>(tmA, tmB, tmC, tmP, p, grid, s);
-    if (v.block_n == 128) return launch_pair<4, false, false, 128>(tmA, tmB, tmC, tmP, p, grid, s);
-  }
+  if (v.esize == 4 && v.block_n == 256)
+    return launch_pair_majors<4, 256>(v, tmA, tmB, tmC, tmP, p, grid, s);
+  if (v.esize == 4 && v.block_n == 128)
+    return launch_pair_majors<4, 128>(v, tmA, tmB, tmC, tmP, p, grid, s);
   return cudaErrorInvalidValue;
 }
 

@@ -172,10 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < G::K_STEPS; ++kk) {
             // K-major: step 32 bytes along the swizzled row; MN-major: step UMMA_K rows.
             const uint64_t ad =
-                A_MN ? sdesc_sw128(a_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
+                A_MN ? sdesc_sw128(a_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES,
+                                  sdesc_mn_sbo<ESIZE>(), sdesc_mode<ESIZE, true>())
                      : sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd =
-                B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES, 1024)
+                B_MN ? sdesc_sw128(b_base + kk * G::UMMA_K * kRowBytes, G::PANEL_BYTES,
+                                  sdesc_mn_sbo<ESIZE>(), sdesc_mode<ESIZE, true>())
                      : sdesc_sw128(b_base + kk * 32, 16, 1024);
             const uint32_t accumulate = (kb | kk) != 0;
             if (ESIZE == 2)
@@ -297,11 +299,9 @@ cudaError_t tc_launch(const TcVariant &v, const CUtensorMap &tmA, const CUtensor
   if (v.exact || v.f16acc) return tc_chunk_launch(v.f16acc, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.pair) return tc2_launch(v, tmA, tmB, tmC, tmP, p, grid, s);
   if (v.esize == 2 && v.block_n == 256) return launch_majors<2, 256>(v, tmA, tmB, tmC, p, grid, s);
-  if (v.esize == 4 && v.block_n == 256 && !v.a_mn && !v.b_mn)
-    return launch_one<4, false, false, 256>(tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 4 && v.block_n == 256) return launch_majors<4, 256>(v, tmA, tmB, tmC, p, grid, s);
   if (v.esize == 2 && v.block_n == 128) return launch_majors<2, 128>(v, tmA, tmB, tmC, p, grid, s);
-  if (v.esize == 4 && v.block_n == 128 && !v.a_mn && !v.b_mn)
-    return launch_one<4, false, false, 128>(tmA, tmB, tmC, p, grid, s);
+  if (v.esize == 4 && v.block_n == 128) return launch_majors<4, 128>(v, tmA, tmB, tmC, p, grid, s);
   return cudaErrorInvalidValue;
 }
 

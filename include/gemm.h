@@ -197,10 +197,14 @@ typedef enum {
   GEMM_OPT_STAGE_K = 12,        /* 128-byte K-blocks per pipeline stage of the CTA-pair
                                    kernel: 0 auto, 1, or 2 (K-major 16-bit operands only;
                                    otherwise GEMM_ERR_UNSUPPORTED at run time) */
-  GEMM_OPT_TILE_ROWS = 13       /* rows of A per CTA of the CTA-pair kernel (its tile has
+  GEMM_OPT_TILE_ROWS = 13,      /* rows of A per CTA of the CTA-pair kernel (its tile has
                                    twice as many): 0 = 128, or a multiple of 8 in [64, 128]
                                    (K-major A and the fp32 accumulator only; otherwise
                                    GEMM_ERR_UNSUPPORTED at run time) */
+  GEMM_OPT_TF32_TRANSPOSE = 14  /* tf32 mode, an MN-major fp32 operand (row-major B,
+                                   column-major A): 0 = the tensor cores read it in place
+                                   (128-byte swizzle with 32-byte atoms), 1 = copy it
+                                   transposed into K-major form first */
 } gemm_option_t;
 
 /* Set a per-handle option; INVALID_ARG for an unknown option or bad value. */

@@ -153,13 +153,23 @@ def test_plan_fp32_modes():
     a, b = t((4096, 4096), torch.float32), t((4096, 4096), torch.float32)
     p = g.plan(a, b, precision="tf32")
     assert p["path"] == "tcgen05" and p["tile_k"] == 32 and p["k_iters"] == 128
-    # The tf32 instruction reads K-major operands only: a row-major B is transposed into
-    # the workspace; a row-major A is already K-major and read in place.
-    assert p["stage_a"] == 0 and p["stage_b"] == 1 and p["b_mn_major"] == 0
-    assert p["workspace_bytes"] == 4096 * 4096 * 4
+    # The tensor cores read a row-major (MN-major) tf32 B in place, in the 128-byte swizzle
+    # with 32-byte atoms; a row-major A is K-major and read in place too.
+    assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["b_mn_major"] == 1
+    assert p["workspace_bytes"] == 0
     p = g.plan(t((100, 60), torch.float32, "col"), t((60, 50), torch.float32, "col"),
                precision="tf32")
-    assert p["stage_a"] == 1 and p["a_mn_major"] == 0 and p["stage_b"] == 0
+    assert p["stage_a"] == 0 and p["a_mn_major"] == 1 and p["stage_b"] == 0
+    # GEMM_OPT_TF32_TRANSPOSE = 1: MN-major tf32 operands are copied K-major first
+    h = g.Gemm.__new__(g.Gemm)
+    hh = ctypes.c_void_p()
+    if g.lib().gemm_create(ctypes.byref(hh), 0) == 0:  # only with a GPU; else plan by options
+        h._h = hh
+        h.set_option("tf32_transpose", 1)
+        p = g.plan(a, b, precision="tf32", handle=h)
+        assert p["stage_b"] == 1 and p["b_mn_major"] == 0
+        assert p["workspace_bytes"] == 4096 * 4096 * 4
+        h.close()
     for prec in ("exact", "default"):
         # Exact fp32: both operands split into tf32 [hi | lo] parts (2K columns each), read
         # as three K-long products.

@@ -384,6 +384,37 @@ def test_fp32_4096_modes(h, precision, force_path):
     full_size_check(p, c)
 
 
+@pytest.mark.parametrize("a_layout,b_layout", [("row", "row"), ("col", "col"), ("col", "row")])
+def test_tf32_mn_major_in_place_and_transposed(h, a_layout, b_layout):
+    # An MN-major fp32 operand in tf32 mode is read in place by the tensor cores (128-byte
+    # swizzle with 32-byte atoms); GEMM_OPT_TF32_TRANSPOSE = 1 copies it K-major first.
+    # Both are compared with the oracle on a ragged problem of several tiles, and with the
+    # exact integer product.
+    import dense_tiled_gemm_05_gb300 as g
+    A = W.make_operand(1500, 1000, "f32", a_layout, 61)
+    B = W.make_operand(1000, 1300, "f32", b_layout, 62)
+    p = W.Problem("tf32_%s_%s" % (a_layout, b_layout), A, B, "f32", "tf32")
+    q = W.integer_problem(700, 900, 1000, "f32", seed=63, a_layout=a_layout, b_layout=b_layout,
+                          precision="tf32")
+    C64, D = oracle_rows(p)
+    outs = []
+    for transpose in (0, 1):
+        h2 = g.Gemm(0)
+        h2.set_option("tf32_transpose", transpose)
+        plan = h2.plan(to_device(p.A), to_device(p.B), out_dtype="f32", precision="tf32")
+        assert plan["a_mn_major"] == (a_layout == "col" and not transpose)
+        assert plan["b_mn_major"] == (b_layout == "row" and not transpose)
+        assert plan["stage_b"] == (b_layout == "row" and transpose == 1)
+        c = run_gpu(h2, p)
+        assert rel_err(c, C64, D) <= tolerance(p)
+        outs.append(c)
+        ci = run_gpu(h2, q)
+        assert torch.equal(ci.cpu().to(torch.int64), q.A.to(torch.int64) @ q.B.to(torch.int64))
+        h2.close()
+    scale = torch.from_numpy(D).to(outs[0].device).clamp_min(1e-30)
+    assert float(((outs[0].double() - outs[1].double()).abs() / scale).max()) <= 2 * tolerance(p)
+
+
 def test_bf16_8192(h):
     p = W.bf16_square(8192, seed=5)
     c = run_gpu(h, p)

@@ -46,12 +46,13 @@ def test_noalloc_matches_run_ex_on_calls_in_a_row(g):
     # The allocation-free path computes whole tiles only (no split-K workspace); compare
     # with the handle path on the same schedule so the bits must agree.
     h.set_option("stream_k", 1)
-    # All need scratch: fp16 rows of 1025 elements are not 16-byte multiples, a row-major B
-    # in tf32 mode is transposed into K-major form, and exact fp32 splits both operands
-    # into tf32 hi and lo parts. The tf32 problem runs twice: once with the array's own
-    # status word, once with the caller's, so a timeout on that kernel would be seen.
-    problems = [(W.ragged(1023, 1000, 1025), True), (W.fp32_square(1000, "tf32", seed=21), False),
-                (W.fp32_square(1000, "tf32", seed=21), True),
+    # All need scratch: fp16 rows of 1025 elements and fp32 rows of 1001 are not 16-byte
+    # multiples (staged copies), and exact fp32 splits both operands into tf32 hi and lo
+    # parts. The tf32 problem runs twice: once with the array's own status word, once with
+    # the caller's, so a timeout on that kernel would be seen.
+    tf32 = W.Problem("tf32_1000x1000x1001", W.make_operand(1000, 1001, "f32", "row", 42),
+                     W.make_operand(1001, 1000, "f32", "row", 43), "f32", "tf32")
+    problems = [(W.ragged(1023, 1000, 1025), True), (tf32, False), (tf32, True),
                 (W.ragged(1000, 700, 1025, seed=22, dtype="f32"), True),
                 (W.ragged(1023, 1000, 1025), True)]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -78,10 +79,11 @@ def test_noalloc_matches_run_ex_on_calls_in_a_row(g):
 
 
 def test_noalloc_rejects_staging_beyond_its_array(g):
-    # A row-major 4096 x 4096 fp32 B in tf32 mode needs a 64 MiB transposed copy, more
-    # than the 32 MiB array: refused before anything is launched, C untouched.
+    # A 4096 x 4097 fp32 B (rows of 16388 bytes, not a 16-byte multiple) needs a 64 MiB
+    # staged copy, more than the 32 MiB array: refused before anything is launched, C
+    # untouched.
     a = torch.zeros(64, 4096, dtype=torch.float32, device="cuda")
-    b = torch.zeros(4096, 4096, dtype=torch.float32, device="cuda")
+    b = torch.zeros(4096, 4097, dtype=torch.float32, device="cuda")[:, :4096]
     out = torch.full((64, 4096), 7.0, dtype=torch.float32, device="cuda")
     rc = noalloc(g, a, b, out, "tf32")
     assert rc == 2  # GEMM_ERR_UNSUPPORTED
