@@ -64,34 +64,63 @@ __global__ void __launch_bounds__(256) split2_rows_kernel(const float *__restric
   }
 }
 
-// The same operand stored the other way, X[r][k] = src[k * lds + r]: a CTA moves 32 lines
-// of k by 512 contiguous bytes of r through shared memory (the strip transpose of the
-// staging copy), so both the reads and the split writes are long contiguous runs.
+// The same operand stored the other way, X[r][k] = src[k * lds + r]: a CTA moves a tile
+// of 32 k by 128 r through shared memory. Reads are 16-byte loads, eight lanes covering
+// 128 contiguous bytes of one k-line; writes are 16-byte stores, eight lanes covering the
+// 128 bytes of hi (and of lo) of one output row. In shared memory element (r, k) sits at
+// r * 32 + (k ^ 4 * ((r / 4) % 8)): the XOR moves whole 4-float groups, so a row's four
+// consecutive k stay one 16-byte word, and both the scalar stores of the load phase and
+// the 16-byte loads of the write phase hit 32 different banks.
 __global__ void __launch_bounds__(256) split2_cols_kernel(const float *__restrict__ src,
                                                           int64_t lds, float *__restrict__ dst,
                                                           int64_t ldd, int64_t R, int64_t K,
-                                                          int64_t Kp) {
-  constexpr int S = 4;  // 32-float pieces per strip line (512 bytes)
-  __shared__ float tile[32][32 * S + 1];
-  const int tx = threadIdx.x, ty = threadIdx.y;
+                                                          int64_t Kp, bool vec) {
+  __shared__ __align__(16) float tile[128 * 32];
+  const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+  const int sub = lane / 8, q = lane % 8;  // 4 lines x 8 four-float groups per warp access
+  auto at = [](int r, int k) { return r * 32 + (k ^ (4 * ((r >> 2) & 7))); };
   for (int64_t k0 = static_cast<int64_t>(blockIdx.y) * 32; k0 < Kp;
        k0 += static_cast<int64_t>(gridDim.y) * 32) {
-    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32 * S; r0 < R;
-         r0 += static_cast<int64_t>(gridDim.x) * 32 * S) {
-      for (int j = ty; j < 32; j += blockDim.y) {
-        const int64_t k = k0 + j;
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * 128; r0 < R;
+         r0 += static_cast<int64_t>(gridDim.x) * 128) {
+      // load: warp w reads k-lines 4w..4w+3; pass i covers r 32i..32i+31
+      const int kl = 4 * w + sub;
+      const int64_t k = k0 + kl;
 #pragma unroll
-        for (int s = 0; s < S; ++s) {
-          const int64_t r = r0 + s * 32 + tx;
-          if (r < R) tile[j][s * 32 + tx] = k < K ? src[k * lds + r] : 0.f;
+      for (int i = 0; i < 4; ++i) {
+        const int rl = 32 * i + 4 * q;
+        const int64_t r = r0 + rl;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < K) {
+          const float *p = src + k * lds + r;
+          if (vec && r + 3 < R) {
+            x = *reinterpret_cast<const float4 *>(p);
+          } else {
+            if (r < R) x.x = p[0];
+            if (r + 1 < R) x.y = p[1];
+            if (r + 2 < R) x.z = p[2];
+            if (r + 3 < R) x.w = p[3];
+          }
         }
+        tile[at(rl + 0, kl)] = x.x;
+        tile[at(rl + 1, kl)] = x.y;
+        tile[at(rl + 2, kl)] = x.z;
+        tile[at(rl + 3, kl)] = x.w;
       }
       __syncthreads();
+      // write: pass i covers output rows 32i + 4w + sub, four k per lane
 #pragma unroll
-      for (int s = 0; s < S; ++s) {
-        for (int j = ty; j < 32; j += blockDim.y) {
-          const int64_t r = r0 + s * 32 + j, k = k0 + tx;
-          if (r < R && k < Kp) put2(dst, ldd, Kp, r, k, tile[tx][s * 32 + j]);
+      for (int i = 0; i < 4; ++i) {
+        const int rl = 32 * i + 4 * w + sub;
+        const int64_t r = r0 + rl;
+        if (r < R) {
+          const float4 x = *reinterpret_cast<const float4 *>(&tile[at(rl, 4 * q)]);
+          const float4 hi = make_float4(tf32_rn(x.x), tf32_rn(x.y), tf32_rn(x.z), tf32_rn(x.w));
+          const float4 lo = make_float4(tf32_rn(x.x - hi.x), tf32_rn(x.y - hi.y),
+                                        tf32_rn(x.z - hi.z), tf32_rn(x.w - hi.w));
+          float *row = dst + r * ldd + k0 + 4 * q;
+          *reinterpret_cast<float4 *>(row) = hi;
+          *reinterpret_cast<float4 *>(row + Kp) = lo;
         }
       }
       __syncthreads();
@@ -115,11 +144,12 @@ cudaError_t split2_launch(const float *src, int64_t lds, bool k_contig, float *d
     split2_rows_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, s>>>(
         src, lds, dst, ldd, R, K, Kp, vec);
   } else {
-    const dim3 block(32, 8);
+    // 16-byte loads need a 16-byte aligned source and a pitch of whole 16-byte words
+    const bool vec = reinterpret_cast<uintptr_t>(src) % 16 == 0 && lds % 4 == 0;
     const int64_t gx = (R + 127) / 128, gy = Kp / 32;
     const dim3 grid(static_cast<unsigned>(gx < 4096 ? gx : 4096),
                     static_cast<unsigned>(gy < 4096 ? gy : 4096));
-    split2_cols_kernel<<<grid, block, 0, s>>>(src, lds, dst, ldd, R, K, Kp);
+    split2_cols_kernel<<<grid, 256, 0, s>>>(src, lds, dst, ldd, R, K, Kp, vec);
   }
   return cudaGetLastError();
 }
