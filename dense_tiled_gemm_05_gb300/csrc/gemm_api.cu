@@ -118,7 +118,7 @@ GEMM_API gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64
       h->max_ctas = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_FAULT_STALL_PRODUCER:
-      if (v < 0 || v > 1) return GEMM_ERR_INVALID_ARG;
+      if (v < 0 || v > (int64_t{1} << 24)) return GEMM_ERR_INVALID_ARG;
       h->stall_producer = static_cast<int>(v);
       return GEMM_OK;
     case GEMM_OPT_FORCE_STAGING:

@@ -10,8 +10,18 @@
 
 namespace gemm_gb300 {
 
-// Debug flags carried into the tensor-core kernel.
-enum : int { kDebugStallProducer = 1 };
+// Debug flags carried into the tensor-core kernel (test hooks of
+// GEMM_OPT_FAULT_STALL_PRODUCER): bit 0, every loader issues nothing; else bits 8.. give a
+// number of stage fills after which a loader stops, that of CTA rank 1 of a pair when bit 1
+// is set, of rank 0 otherwise (the single-CTA kernel's loader either way).
+enum : int { kDebugStallProducer = 1, kDebugStallRank1 = 2, kDebugStallAfterShift = 8 };
+
+// Stage fills after which this CTA's loader stops under the test hook (-1: never).
+inline __host__ __device__ int stall_after_fills(int debug_flags, int rank) {
+  const int n = debug_flags >> kDebugStallAfterShift;
+  if (n <= 0) return -1;
+  return ((debug_flags & kDebugStallRank1) ? 1 : 0) == rank ? n : -1;
+}
 // TcParams::l2_once bits: the operand is read by one tile column (A) or row (B) only.
 enum : int { kL2OnceA = 1, kL2OnceB = 2 };
 

@@ -242,6 +242,14 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "tcgen05 launch");
 }
 
+// GEMM_OPT_FAULT_STALL_PRODUCER value -> kernel debug flags: 1, no loads at all; v >= 2,
+// the loader of CTA rank (v & 1) stops after v >> 1 stage fills.
+static int stall_flags(int v) {
+  if (v == 1) return kDebugStallProducer;
+  if (v >= 2) return ((v >> 1) << kDebugStallAfterShift) | ((v & 1) ? kDebugStallRank1 : 0);
+  return 0;
+}
+
 gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStream_t s,
                       bool record_events) {
   const gemm_plan_info_t &I = pl.info;
@@ -294,7 +302,7 @@ gemm_status_t execute(gemm_handle_t h, const Problem &P, const Plan &pl, cudaStr
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess)
     return cuda_fail(e, "record the kernel start event");
   st = launch_tc(P, pl, a_ptr, a_ld, b_ptr, b_ld, h->status, h->timeout_us * 1000ull,
-                 pl.group_m, h->stall_producer ? kDebugStallProducer : 0, sk, s);
+                 pl.group_m, stall_flags(h->stall_producer), sk, s);
   if (st != GEMM_OK) return st;
   h->launches += 1;
   if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess)

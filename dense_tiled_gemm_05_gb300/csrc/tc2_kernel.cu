@@ -57,7 +57,8 @@ struct Cfg2 {
   static constexpr int PART_BUFS = OWNER_SLICE / PART_BYTES;  // partial loads in flight
   // + one partial-load barrier per buffer of each epilogue warp
   static constexpr int NUM_BARS = 2 * STAGES + 5 + kEpiWarps * PART_BUFS;
-  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
+  // + TMEM address, abort flag and the four teardown words (see `xs` in the kernel)
+  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 32 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -84,6 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *part_bar = drain + 1;  // [kEpiWarps][PART_BUFS]: owner warps' partial loads
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(part_bar + kEpiWarps * G::PART_BUFS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // Teardown words: [0] stage fills this CTA's loader issued, [1] fills the MMA issuer
+  // consumed (leader), [2] fills the peer's loader issued (the peer writes it into the
+  // leader), [3] whether the other CTA of the pair aborted (written by that CTA).
+  volatile uint32_t *xs = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -102,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     for (int w = 0; w < kEpiWarps * G::PART_BUFS; ++w) mbar_init(&part_bar[w], 1);
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) xs[i] = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -130,8 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
+      uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      const int stop_after = stall_after_fills(p.debug_flags, static_cast<int>(rank));
       // Operand tiles stay in L2 longest, unless only one tile row or column reads them.
       const uint64_t keep = l2_policy_evict_last();
       const uint64_t pol_a = (p.l2_once & kL2OnceA) ? l2_policy_evict_first() : keep;
@@ -154,6 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.k_rotate ? static_cast<int>(static_cast<int64_t>(seg.tile) * p.k_rotate % len) : 0;
         for (int i = 0; i < len; ++i) {
           const int kb = seg.kb_begin + (i + rot < len ? i + rot : i + rot - len);
+          if (stop_after >= 0 && issued >= static_cast<uint32_t>(stop_after)) {
+            ok = false;  // test hook: this loader stops here, copies still in flight
+            break;
+          }
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
@@ -185,18 +196,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d_pair_hint(b_dst + j * G::B_BOX_BYTES, &tmB, fb, k0 + j * G::BOX_K, n0,
                                     pol_b);
           }
+          ++issued;
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      xs[0] = issued;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer (leader)
     if (leader && lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, consumed = 0;
       bool ok = true;
       WorkIter work(sched, cluster_id);
       SkSegment seg;
@@ -209,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          ++consumed;
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t b_base = a_base + G::A_BYTES;
@@ -244,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_pair(drain);  // every MMA issued above completes before TMEM is released
       drain_wait(drain, 0, p.timeout_ns);
+      xs[1] = consumed;
     }
     __syncwarp();
   } else {
@@ -294,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint64_t *bars = part_bar + e * G::PART_BUFS;
           const int nsrc = seg.last_src - seg.first_src + 1;
           // Wait for partial i's flag, then load it into buffer i % PART_BUFS.
+          int fetched = 0, added = 0;  // partial loads issued, and waited for
           auto fetch = [&](int i) {
             const int w = seg.first_src + i;
             bool f = wait_flag(p.sk_flags + (w * 2 + rank) * 4 + quarter, epoch, wd);
@@ -309,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem_u32(buf + c * kStoreBufBytes), &tmP, smem_u32(&bars[b]), c * 32,
                             part_row0(w));
             }
+            ++fetched;
             return true;
           };
           for (int i = 0; ok && i < nsrc && i < G::PART_BUFS; ++i) ok = fetch(i);
@@ -316,8 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = i % G::PART_BUFS;
             ok = mbar_wait(&bars[b], (part_phase >> b) & 1u, wd);
             ok = __all_sync(0xffffffffu, ok);
-            part_phase ^= 1u << b;
             if (!ok) break;
+            part_phase ^= 1u << b;
+            ++added;
             add_partial_into_tmem<G::BN>(t_row, slice + b * G::PART_BYTES, lane);
             if (i + G::PART_BUFS < nsrc) {
               __syncwarp();               // every lane has read buffer b
@@ -325,7 +343,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = fetch(i + G::PART_BUFS);
             }
           }
-          if (!ok) break;
+          if (!ok) {
+            // Partial loads already issued may still be landing in this warp's slice: let
+            // them complete (each buffer holds at most one) before the CTA can leave.
+            if (lane == 0)
+              for (int i = added; i < fetched; ++i) {
+                const int b = i % G::PART_BUFS;
+                drain_wait(&bars[b], (part_phase >> b) & 1u, p.timeout_ns);
+                part_phase ^= 1u << b;
+              }
+            __syncwarp();
+            break;
+          }
         }
         if (valid <= 0) {
           // no row of the tile in this warp's lanes
@@ -358,15 +387,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (*abort_flag && warp == 0 && lane == 0) {
-    // After an abort, give TMA copies already issued time to land before the CTA leaves
-    // (their barrier may live in the other CTA, so they cannot be waited on here).
-    const uint64_t t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 200000) __nanosleep(1000);
+  // Tell the other CTA whether this one aborted, and the leader how many stage fills the
+  // peer's loader issued (the peer's copies complete on the leader's barriers).
+  if (threadIdx.x == 0) {
+    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(&xs[3])), rank ^ 1u),
+                          *abort_flag ? 1u : 0u);
+    if (!leader) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(&xs[2])), 0), xs[0]);
   }
-  __syncwarp();
   tc_fence_before();
-  cluster_sync();  // both CTAs done: no more remote arrivals, all MMAs drained
+  cluster_sync();  // both CTAs done, all MMAs drained; abort states exchanged
+  if (*abort_flag || xs[3]) {
+    // After an abort, neither CTA leaves while a copy it issued may still land in its
+    // shared memory: the leader accounts for every outstanding fill and waits for it.
+    if (leader && threadIdx.x == 0)
+      drain_pair_fills<G::STAGES>(full, xs[1], xs[0], xs[2],
+                                  static_cast<uint32_t>(p.cta_rows * G::BK * ESIZE + G::B_BYTES),
+                                  p.timeout_ns);
+    cluster_sync();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, G::TMEM_COLS);

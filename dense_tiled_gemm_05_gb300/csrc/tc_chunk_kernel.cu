@@ -62,7 +62,8 @@ struct CfgX {
   static constexpr int EPI_BYTES = kXEpiWarps * kStoreBufBytes;  // one staging box per warp
   static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
-  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
+  // + TMEM address, abort flag and the four teardown words (see `xs` in the kernel)
+  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 32 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int COLS = 128;  // columns per epilogue thread
   static_assert(K_STEPS == 4, "four MMAs per K-block");
@@ -158,6 +159,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
   uint64_t *drain = tmem_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // Teardown words, as in the CTA-pair kernel: [0] stage fills this CTA's loader issued,
+  // [1] fills the MMA issuer consumed (leader), [2] the peer's issued fills (written by the
+  // peer into the leader), [3] whether the other CTA aborted.
+  volatile uint32_t *xs = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) xs[i] = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -212,8 +218,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
+      uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      const int stop_after = stall_after_fills(p.debug_flags, static_cast<int>(rank));
       const uint64_t keep = l2_policy_evict_last();  // operand tiles stay in L2 longest
       WorkIter work(sched, cluster_id);
       SkSegment seg;
@@ -223,6 +230,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const int m0 = pm * (2 * G::BM) + static_cast<int>(rank) * G::BM;
         const int n0 = pn * G::BN + static_cast<int>(rank) * G::BN_HALF;
         for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+          if (stop_after >= 0 && issued >= static_cast<uint32_t>(stop_after)) {
+            ok = false;  // test hook: this loader stops here, copies still in flight
+            break;
+          }
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
@@ -239,18 +250,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
           }
           tma_load_2d_pair_hint(a_dst, &tmA, fb, xa, m0, keep);
           tma_load_2d_pair_hint(a_dst + G::A_BYTES, &tmB, fb, xb, n0, keep);
+          ++issued;
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      xs[0] = issued;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer (leader)
     if (leader && lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, consumed = 0;
       bool ok = true;
       // Four MMAs per K-block. When chunks are whole K-blocks (always in exact mode) the
       // chunk decisions are taken once per K-block and the four MMAs issue back to back:
@@ -291,6 +304,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 ok = false;
                 break;
               }
+              ++consumed;
               tc_fence_after();
               const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
               const uint32_t b_base = a_base + G::A_BYTES;
@@ -318,6 +332,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
             ok = false;
             break;
           }
+          ++consumed;
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * G::STAGE_BYTES);
           const uint32_t b_base = a_base + G::A_BYTES;
@@ -349,6 +364,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       }
       mma_commit_pair(drain);
       drain_wait(drain, 0, p.timeout_ns);
+      xs[1] = consumed;
     }
     __syncwarp();
   } else {
@@ -478,13 +494,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
   }
 
   __syncthreads();
-  if (*abort_flag && warp == 0 && lane == 0) {
-    const uint64_t t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 200000) __nanosleep(1000);
+  // As in the CTA-pair kernel: exchange abort states; after an abort the leader accounts
+  // for and waits for every stage fill either CTA's loader issued before either leaves.
+  if (threadIdx.x == 0) {
+    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(&xs[3])), rank ^ 1u),
+                          *abort_flag ? 1u : 0u);
+    if (!leader) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(&xs[2])), 0), xs[0]);
   }
-  __syncwarp();
   tc_fence_before();
   cluster_sync();
+  if (*abort_flag || xs[3]) {
+    if (leader && threadIdx.x == 0)
+      drain_pair_fills<G::STAGES>(full, xs[1], xs[0], xs[2], G::STAGE_BYTES, p.timeout_ns);
+    cluster_sync();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, G::TMEM_COLS);

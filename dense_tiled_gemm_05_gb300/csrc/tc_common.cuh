@@ -41,6 +41,32 @@ static __device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity, u
   }
 }
 
+// Teardown of a CTA pair after an abort. Both CTAs' TMA loads signal the leader's full
+// barriers: a stage fill is complete when the leader's producer has arrived (expecting the
+// bytes of both CTAs) and both CTAs' bytes have landed. Fills numbered `consumed` and on
+// (the MMA issuer waited for all earlier ones) may still be in flight: the leader issued
+// `leader_issued` fills, the peer `peer_issued`, and the two differ when one producer
+// stopped first. For each outstanding fill the leader completes the barrier's accounting
+// for the side that never issued it -- the peer's bytes it still expects, or the arrival
+// and the peer's bytes when only the peer issued -- and waits (bounded) for the phase, so
+// every copy either CTA issued has landed when this returns. At most STAGES fills are
+// outstanding (a producer reuses a stage only after the MMAs have consumed it), so each
+// stage has at most one outstanding phase.
+template <int STAGES>
+__device__ __noinline__ void drain_pair_fills(uint64_t *full, uint32_t consumed,
+                                              uint32_t leader_issued, uint32_t peer_issued,
+                                              uint32_t peer_bytes, uint64_t timeout_ns) {
+  const uint32_t end = leader_issued > peer_issued ? leader_issued : peer_issued;
+  for (uint32_t i = consumed; i < end; ++i) {
+    uint64_t *bar = &full[i % STAGES];
+    if (i >= leader_issued)
+      mbar_arrive_expect_tx(bar, peer_bytes);  // only the peer issued this fill
+    else if (i >= peer_issued)
+      mbar_complete_tx(bar, peer_bytes);  // the peer's part of this fill never comes
+    drain_wait(bar, (i / STAGES) & 1, timeout_ns);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(uint32_t a, uint32_t b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(a), __uint_as_float(b));
   return *reinterpret_cast<uint32_t *>(&h);

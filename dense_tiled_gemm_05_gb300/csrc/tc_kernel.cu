@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = (p.debug_flags & kDebugStallProducer) == 0;
+      // test hook: the loader stops after this many stage fills (-1: never)
+      const int stop_after = stall_after_fills(p.debug_flags & ~kDebugStallRank1, 0);
       // Operand tiles stay in L2 longest, unless only one tile row or column reads them.
       const uint64_t keep = l2_policy_evict_last();
       const uint64_t pol_a = (p.l2_once & kL2OnceA) ? l2_policy_evict_first() : keep;
@@ -119,6 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.k_rotate ? static_cast<int>(static_cast<int64_t>(tile) * p.k_rotate % p.k_blocks) : 0;
         for (int kb_i = 0; kb_i < p.k_blocks; ++kb_i) {
           const int kb = kb_i + rot < p.k_blocks ? kb_i + rot : kb_i + rot - p.k_blocks;
+          if (stop_after >= 0 && issued >= static_cast<uint32_t>(stop_after)) {
+            ok = false;  // test hook: the loader stops here, copies still in flight
+            break;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;

@@ -175,9 +175,12 @@ typedef enum {
   GEMM_OPT_FORCE_PATH = 1,      /* 0 auto, 1 tensor cores, 2 fp32 FMA kernel (any input dtype) */
   GEMM_OPT_GROUP_M = 2,         /* tile rows per raster group of the persistent schedule (>= 1) */
   GEMM_OPT_MAX_CTAS = 3,        /* cap on persistent CTAs (0 = one per SM) */
-  GEMM_OPT_FAULT_STALL_PRODUCER = 4, /* test hook: the tensor-core kernel's loader issues
+  GEMM_OPT_FAULT_STALL_PRODUCER = 4, /* test hook: 1 = the tensor-core kernel's loader issues
                                         nothing, so the consumers' bounded waits expire and the
-                                        kernel reports GEMM_ERR_TIMEOUT; 0 = off */
+                                        kernel reports GEMM_ERR_TIMEOUT; v >= 2 = the loader of
+                                        CTA rank (v & 1) of a pair (the single CTA's loader)
+                                        stops after v >> 1 stage fills, with copies still in
+                                        flight; 0 = off */
   GEMM_OPT_FORCE_STAGING = 5,   /* 1 = stage A and B through the workspace even when aligned */
   GEMM_OPT_CTA_PAIR = 6,        /* tensor-core tiles: 0 auto, 1 single-CTA (128 rows),
                                    2 CTA-pair (256 rows, cta_group::2 on two SMs) */

@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a GPU fault: the tensor-core kernel's loader
-is told to issue nothing, so the MMA and epilogue roles' bounded mbarrier waits expire
-after a short limit; the kernel records GEMM_ERR_TIMEOUT in the handle's status word,
-releases its TMEM and returns. The same context then runs a normal GEMM correctly."""
+is told to issue nothing, or to stop after some stage fills with copies still in flight,
+so the MMA and epilogue roles' bounded mbarrier waits expire after a short limit; the
+kernel records GEMM_ERR_TIMEOUT in the handle's status word, lets every copy it issued
+land, releases its TMEM and returns. The same context then runs a normal GEMM correctly."""
 import pytest
 import torch
 
@@ -90,6 +91,47 @@ def test_split_k_after_a_timeout(g):
     h.set_option("fault_stall_producer", 0)
     for _ in range(3):
         c = h.matmul(a, b, out_dtype="f32")
+        assert h.status() == 0
+        assert torch.equal(c.cpu().to(torch.int64), ref)
+    h.close()
+
+
+@pytest.mark.parametrize("kind,who", [("pair", 0), ("pair", 1), ("single", 0), ("exact", 0),
+                                      ("exact", 1), ("pair_split", 0), ("pair_split", 1)])
+def test_loader_stops_with_copies_in_flight(g, kind, who):
+    # The loader of one CTA (rank `who` of a pair) stops after 20 stage fills, so the other
+    # CTA's loader keeps issuing until the ring is full and the MMA issuer's bounded wait
+    # expires with copies of both CTAs still in flight. Before either CTA of a pair leaves,
+    # the leader accounts for every outstanding fill (the bytes that never come, or the
+    # missing arrival) and waits for the copies that were issued. Nothing faults or hangs:
+    # the kernel reports GEMM_ERR_TIMEOUT and the same context then computes correctly.
+    dtype = "f32" if kind == "exact" else "bf16"
+    # (every cluster of the split product still takes more than 20 K-blocks)
+    M, N, K = {"exact": (700, 600, 1500), "pair_split": (4096, 2048, 4096)}.get(kind, (1100, 900, 4096))
+    p = W.integer_problem(M, N, K, dtype, seed=61 + who, b_layout="col")
+    a, b = to_device(p.A), to_device(p.B)
+    ref = p.A.to(torch.int64) @ p.B.to(torch.int64)
+    h = g.Gemm(0)
+    h.set_option("cta_pair", 1 if kind == "single" else 2)
+    if kind == "pair_split":
+        h.set_option("stream_k", 2)
+        assert h.plan(a, b, out_dtype="f32")["split_tiles"] > 0
+    plan = h.plan(a, b, out_dtype="f32", precision=p.precision)
+    assert plan["k_iters"] > 20 and plan["cta_pair"] == (0 if kind == "single" else 1)
+    h.set_option("wait_timeout_us", 20000)
+    h.set_option("fault_stall_producer", 2 * 20 + who)
+    for _ in range(2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        h.matmul(a, b, out_dtype="f32", precision=p.precision)
+        e1.record()
+        assert h.status() == 6  # GEMM_ERR_TIMEOUT
+        # One 20 ms limit expires; the teardown's waits for the copies in flight end at once
+        # (each would take another 20 ms if the outstanding fills were miscounted).
+        assert e0.elapsed_time(e1) < 80.0, e0.elapsed_time(e1)
+    h.set_option("fault_stall_producer", 0)
+    for _ in range(2):
+        c = h.matmul(a, b, out_dtype="f32", precision=p.precision)
         assert h.status() == 0
         assert torch.equal(c.cpu().to(torch.int64), ref)
     h.close()
