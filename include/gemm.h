@@ -36,7 +36,8 @@
  *
  * Precision (fp32 inputs only): GEMM_PREC_DEFAULT means GEMM_PREC_EXACT_FP32;
  * GEMM_PREC_TF32 runs the tensor cores on tf32 operands (the low 13 mantissa bits
- * of each fp32 input are ignored; max |err| <= 2e-3 * sum_k |a_ik b_kj|).
+ * of each fp32 input are ignored; max |err| <= 2e-3 * sum_k |a_ik b_kj|), reading
+ * row- and column-major operands alike in place.
  * GEMM_PREC_EXACT_FP32 keeps fp32 accuracy (max |err| <= 1e-6 * sum_k |a_ik b_kj|
  * on the library's tests): each operand is split into two tf32 parts and the
  * three significant partial products run on the tensor cores, accumulating in
@@ -220,7 +221,8 @@ GEMM_API gemm_status_t gemm_get_launch_count(gemm_handle_t h, uint64_t *count);
  * cudaEvent_t handles (created by the caller, on this handle's device), every later
  * gemm_run / gemm_run_ex / gemm_run_strided call on this handle records start_event on
  * its stream immediately before it launches the GEMM kernel itself -- after any staging
- * copies (misaligned operands, transposed tf32 operands, the hi/lo split of exact fp32)
+ * copies (misaligned operands, transposed copies under GEMM_OPT_TF32_TRANSPOSE or for the
+ * fp16 accumulator, the hi/lo split of exact fp32)
  * -- and end_event immediately after it, so that the caller can time that kernel apart
  * from the copies with cudaEventElapsedTime. Both NULL turns the hook off (the default).
  * The events stay owned by the caller, who must keep them alive while the hook is set.
