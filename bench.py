@@ -626,6 +626,8 @@ def timed_steps(h, step, n, stream, dev, period_ms=200, dist=None, events=True):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index, period_ms) as clocks:
+        # an NVTX range marks the timed region for a timeline profiler (no-op without one)
+        torch.cuda.nvtx.range_push("timed steps (%d%s)" % (n, ", per-step events" if events else ""))
         t0.record(stream)
         if events:
             for i in range(n):
@@ -638,6 +640,7 @@ def timed_steps(h, step, n, stream, dev, period_ms=200, dist=None, events=True):
                 step(i)
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_pop()
     h.set_kernel_events()
     if dist:
         dist.barrier()
@@ -699,9 +702,10 @@ def kernel_name(h, a, b, p):
     return ("tc2_gemm_kernel (CTA pair)" if plan["cta_pair"] else "tc_gemm_kernel (single CTA)"), plan
 
 
-def measure_config(g, dev, name, peaks, peak_src, min_s=0.3, cpu_s=3.0):
+def measure_config(g, dev, name, peaks, peak_src, min_s=0.3, cpu_s=3.0, hot_l2=False):
     """One workload of the target measured in the default run: warm-up, then steps for
-    about `min_s` seconds (at least 50), inputs rotated over buffer sets larger than L2."""
+    about `min_s` seconds (at least 50), inputs rotated over buffer sets larger than L2
+    (with `hot_l2`, also a labelled run on one buffer set, its operands resident in L2)."""
     p, desc, bound = workload(name)
     h = g.Gemm(dev.index)
     stream = torch.cuda.current_stream(dev)
@@ -746,6 +750,25 @@ def measure_config(g, dev, name, peaks, peak_src, min_s=0.3, cpu_s=3.0):
            "dtype": {"bf16": "bf16", "f32": "tf32" if p.precision == "tf32" else "f32"}[p.in_dtype]}
     if bound == "hbm":
         out["hbm_gbs"] = algorithmic_bytes(p) * n / (elapsed_ms / 1e3) / 1e9
+    else:
+        # against the datasheet's dense peak for the input type (bf16 2250 TFLOP/s at the
+        # 2070 MHz maximum clock; tf32 1100; exact fp32 = three tf32 products)
+        ds = DATASHEET_BF16_TFLOPS * (TF32_OVER_BF16 if p.in_dtype == "f32" else 1.0)
+        ds /= 3.0 if bound == "tensor_x3" else 1.0
+        out["datasheet_peak_tflops"] = ds
+        out["pct_of_datasheet_peak"] = 100.0 * out["value"] / ds
+    if hot_l2:
+        # the same operands every step (they stay in L2): labelled, not the config's value
+        def hot(i):
+            h.matmul(sets[0][0], sets[0][1], out=outs[0], precision=p.precision, stream=stream)
+        for i in range(10):
+            hot(i)
+        hot_ms, _, _, _, hot_clocks = timed_steps(h, hot, n, stream, dev, period_ms=50,
+                                                  events=False)
+        out["hot_l2"] = {"value": flops * n / (hot_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                         "ms_per_step": hot_ms / n, "steps": n,
+                         "l2": "one buffer set: operands resident in L2 across steps",
+                         "sm_mhz": hot_clocks.get("sm_mhz")}
     if cpu_s > 0:
         out["cpu_baseline"] = cpu_baseline(p, target_s=cpu_s)
     h.close()
@@ -947,7 +970,8 @@ def main():
         cpu_s = 0.0 if args.no_cpu_baseline else 3.0
         configs = {}
         for name in CONFIG_WORKLOADS:
-            configs[name] = measure_config(g, dev, name, peaks, peak_src, cpu_s=cpu_s)
+            configs[name] = measure_config(g, dev, name, peaks, peak_src, cpu_s=cpu_s,
+                                           hot_l2=name == "bf16_4096")
         configs["ragged_216"] = ragged_measure(g, dev, 50, 5, peaks, peak_src, period_ms=50,
                                                cpu_s=cpu_s)
         line["configs"] = configs
