@@ -24,6 +24,8 @@ inline __host__ __device__ int stall_after_fills(int debug_flags, int rank) {
 }
 // TcParams::l2_once bits: the operand is read by one tile column (A) or row (B) only.
 enum : int { kL2OnceA = 1, kL2OnceB = 2 };
+// TcParams::mn_3d bits: the MN-major operand's tensor map is 3D (one copy per stage).
+enum : int { kMn3dA = 1, kMn3dB = 2 };
 
 // Output tile of the tensor-core kernel: 128 rows (one TMEM lane per row).
 constexpr int kTcBlockM = 128;
@@ -46,6 +48,7 @@ struct TcParams {
   int32_t l2_once;        // kL2OnceA | kL2OnceB: operands loaded as first to evict from L2
   int32_t k_rotate;       // whole tile t starts at K-block (t * k_rotate) mod k_blocks (0: 0)
   int32_t split_kb;       // exact fp32: K-blocks per hi or lo part of the split operands
+  int32_t mn_3d;          // kMn3dA | kMn3dB: MN-major operands loaded by one 3D copy a stage
   // split-K share of the last rounds (CTA-pair kernel; see sk_schedule.h)
   int32_t sk_dp_tiles;    // tiles done whole, round-robin (== tiles: no split)
   float *sk_partials;     // [worker][cta rank][128 rows][block_n] fp32

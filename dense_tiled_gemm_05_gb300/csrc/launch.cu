@@ -79,6 +79,34 @@ bool encode_2d(CUtensorMap *m, int dtype, const void *base, int64_t inner, int64
   return r == CUDA_SUCCESS;
 }
 
+// 3D tensor map over an MN-major operand that loads a CTA's whole slice of a stage with
+// one copy: dims {panel, K, MN / panel} (128-byte panels of M or N, K rows of the stage,
+// the panel index), strides {ld, panel} in bytes, box {panel, k_rows, panels}. The box
+// lands in shared memory panel after panel, each panel k_rows x 128 bytes, which is the
+// layout the 2D loads build one panel at a time. Only for an MN extent that is a whole
+// number of panels: a 3D box has no bound inside a panel, so a partial last panel would
+// read past the operand's rows instead of reading zeros.
+bool encode_3d_panels(CUtensorMap *m, int dtype, const void *base, int64_t mn, int64_t k,
+                      int64_t ld, uint32_t k_rows, uint32_t panels, bool atom32) {
+  EncodeTiledFn fn = encode_fn();
+  const int es = esize_of(dtype);
+  const int64_t panel = 128 / es;
+  if (!fn || mn % panel != 0 || k <= 1) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(panel), static_cast<cuuint64_t>(k),
+                              static_cast<cuuint64_t>(mn / panel)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es), 128};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(panel), k_rows, panels};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, tmap_dtype(dtype), 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  atom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS && log_enabled())
+    std::fprintf(stderr, "[gemm] cuTensorMapEncodeTiled (3D panels) failed (%d)\n",
+                 static_cast<int>(r));
+  return r == CUDA_SUCCESS;
+}
+
 static uint32_t make_idesc(int in_dtype, bool a_mn, bool b_mn, int n, int m) {
   const uint32_t fmt = in_dtype == GEMM_F16 ? 0u : in_dtype == GEMM_BF16 ? 1u : 2u;
   uint32_t d = 0;
@@ -164,6 +192,26 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
       !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
                  b_box_outer, es == 4 && pl.b.mn_major))
     return GEMM_ERR_CUDA;
+  // CTA pairs: an MN-major operand whose M or N is a whole number of 128-byte panels is
+  // loaded with one 3D copy per stage instead of one 2D copy per panel (the loader issues
+  // fewer, larger copies; it kept a tf32 B of four panels a stage behind the MMAs).
+  int32_t mn_3d = 0;
+  if (pl.variant.pair && !pl.variant.exact && !pl.variant.f16acc) {
+    const uint32_t k_rows = static_cast<uint32_t>(pl.variant.kps) * row_elems;
+    CUtensorMap m3;
+    if (pl.a.mn_major && pl.cta_rows == kTcBlockM &&
+        encode_3d_panels(&m3, P.in_dtype, a_ptr, pl.a.k_inner, pl.a.k_outer, a_ld, k_rows,
+                         cta_rows_a / row_elems, es == 4)) {
+      tmA = m3;
+      mn_3d |= kMn3dA;
+    }
+    if (pl.b.mn_major && cta_rows_b % row_elems == 0 &&
+        encode_3d_panels(&m3, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, k_rows,
+                         cta_rows_b / row_elems, es == 4)) {
+      tmB = m3;
+      mn_3d |= kMn3dB;
+    }
+  }
   if (I.tma_store) {
     const uint32_t out_row = 128 / esize_of(P.out_dtype);
     if (!encode_2d(&tmC, P.out_dtype, P.C, P.N, P.M, P.ldc, out_row, 32)) return GEMM_ERR_CUDA;
@@ -193,6 +241,7 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
   tp.chunk_steps = pl.chunk_steps;
   tp.cta_rows = pl.cta_rows;
   tp.split_kb = pl.a.split_hl ? static_cast<int32_t>(pl.a.split_kp / 32) : 0;
+  tp.mn_3d = mn_3d;
   // An operand that only one tile column (A) or one tile row (B) reads is streamed once:
   // its loads go to L2 as first to evict, and whole tiles then start their K-loops at
   // staggered K-blocks, so that tiles running side by side do not all fetch the same

@@ -399,6 +399,18 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtens
       : "memory");
 }
 
+// 3D tiled load (coordinates x innermost, then y, z) into this CTA's shared memory,
+// completion signalled on an mbarrier of either CTA of the pair, under an L2 policy.
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap *m,
+                                                      uint32_t bar, int32_t x, int32_t y,
+                                                      int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
 // An L2 policy under which the lines a load brings in are the last to be evicted. GEMM
 // operand tiles are reused by every tile of a raster group while the output streams
 // through L2 once; keeping the operands resident cut DRAM traffic and, under the power cap,

@@ -500,3 +500,31 @@ def test_north_star_signature_gemm_run(h):
         assert torch.isnan(c[:, p.N:]).all()
         if p.M == 2:  # the pages' printed single-tile result, bit for bit
             assert torch.equal(c[:, :2].cpu(), torch.tensor([[19.0, 22.0], [43.0, 50.0]]))
+
+
+@pytest.mark.parametrize("dtype,precision", [("bf16", "default"), ("f16", "default"),
+                                             ("f32", "tf32")])
+@pytest.mark.parametrize("a_layout,b_layout", [("col", "row"), ("row", "row"), ("col", "col")])
+@pytest.mark.parametrize("block_n,stream_k", [(256, 1), (256, 2), (128, 0)])
+def test_mn_major_panel_loads_integer_exact(h, dtype, precision, a_layout, b_layout, block_n,
+                                            stream_k):
+    # CTA pairs load an MN-major operand whose M or N is a whole number of 128-byte panels
+    # with one 3D copy a stage (all of a CTA's panels at once); other extents keep one 2D
+    # copy a panel. Both must give the exact integer product: extents that are and are not
+    # whole panels (32 tf32 or 64 16-bit elements), ragged K, split-K pieces.
+    import dense_tiled_gemm_05_gb300 as g
+    h2 = g.Gemm(0)
+    h2.set_option("cta_pair", 2)
+    h2.set_option("block_n", block_n)
+    h2.set_option("stream_k", stream_k)
+    shapes = [(512, 512, 1000), (384, 320, 129), (256, 96, 64), (1024, 2048, 777),
+              (640, 192, 1025), (300, 130, 200)]
+    for n, (M, N, K) in enumerate(shapes):
+        p = W.integer_problem(M, N, K, dtype, seed=900 + n, a_layout=a_layout,
+                              b_layout=b_layout, precision=precision)
+        plan = h2.plan(to_device(p.A), to_device(p.B), out_dtype="f32", precision=precision)
+        assert plan["cta_pair"] == 1 and plan["tile_n"] == block_n, plan
+        c = run_gpu(h2, p)
+        assert torch.equal(c.cpu().to(torch.int64), p.A.to(torch.int64) @ p.B.to(torch.int64)), (
+            M, N, K)
+    h2.close()
