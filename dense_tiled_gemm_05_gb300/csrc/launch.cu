@@ -192,11 +192,11 @@ gemm_status_t launch_tc(const Problem &P, const Plan &pl, const void *a_ptr, int
       !encode_2d(&tmB, P.in_dtype, b_ptr, pl.b.k_inner, pl.b.k_outer, b_ld, row_elems,
                  b_box_outer, es == 4 && pl.b.mn_major))
     return GEMM_ERR_CUDA;
-  // CTA pairs: an MN-major operand whose M or N is a whole number of 128-byte panels is
-  // loaded with one 3D copy per stage instead of one 2D copy per panel (the loader issues
-  // fewer, larger copies; it kept a tf32 B of four panels a stage behind the MMAs).
+  // An MN-major operand whose M or N is a whole number of 128-byte panels is loaded with
+  // one 3D copy per stage instead of one 2D copy per panel (the loader issues fewer, larger
+  // copies; one copy per panel kept a tf32 B of four panels a stage behind the MMAs).
   int32_t mn_3d = 0;
-  if (pl.variant.pair && !pl.variant.exact && !pl.variant.f16acc) {
+  if (!pl.variant.exact && !pl.variant.f16acc) {
     const uint32_t k_rows = static_cast<uint32_t>(pl.variant.kps) * row_elems;
     CUtensorMap m3;
     if (pl.a.mn_major && pl.cta_rows == kTcBlockM &&

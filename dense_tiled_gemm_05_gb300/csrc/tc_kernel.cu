@@ -134,14 +134,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_dst = a_dst + G::A_BYTES;
           const uint32_t fb = smem_u32(&full[stage]);
           const int k0 = kb * G::BK;
-          if (A_MN) {
+          if (A_MN && (p.mn_3d & kMn3dA)) {
+            tma_load_3d_hint(a_dst, &tmA, fb, 0, k0, m0 / G::PANEL, pol_a);
+          } else if (A_MN) {
 #pragma unroll
             for (int q = 0; q < G::BM / G::PANEL; ++q)
               tma_load_2d_hint(a_dst + q * G::PANEL_BYTES, &tmA, fb, m0 + q * G::PANEL, k0, pol_a);
           } else {
             tma_load_2d_hint(a_dst, &tmA, fb, k0, m0, pol_a);
           }
-          if (B_MN) {
+          if (B_MN && (p.mn_3d & kMn3dB)) {
+            tma_load_3d_hint(b_dst, &tmB, fb, 0, k0, n0 / G::PANEL, pol_b);
+          } else if (B_MN) {
 #pragma unroll
             for (int q = 0; q < BN / G::PANEL; ++q)
               tma_load_2d_hint(b_dst + q * G::PANEL_BYTES, &tmB, fb, n0 + q * G::PANEL, k0, pol_b);
