@@ -67,6 +67,16 @@ struct Cfg2 {
   static_assert(KPS == 1 || (!A_MN && !B_MN), "wide stages for K-major operands only");
 };
 
+// Wait on a barrier of the operand ring (stage full, stage empty). Their arrivals come
+// from the async units (TMA copies completing, tcgen05.commit), and what the waiting thread
+// does next is issue more async work (MMAs reading the stage, copies refilling it), so an
+// acquire at CTA scope is enough; at cluster scope each wait costs more. Measured on one
+// GB300 (interleaved, order rotated, CUDA events): bf16 4096^3 93.0 -> 90.9 us,
+// 2048^2 x 8192 48.2 -> 46.5, 8192^3 -1 %; tf32 unchanged.
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, const Watchdog &wd) {
+  return mbar_wait(bar, parity, wd);
+}
+
 template <int ESIZE, bool A_MN, bool B_MN, int BN, int KPS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;  // test hook: this loader stops here, copies still in flight
             break;
           }
-          if (!mbar_wait_cluster(&empty[stage], phase ^ 1, wd)) {
+          if (!ring_wait(&empty[stage], phase ^ 1, wd)) {
             ok = false;
             break;
           }
@@ -222,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
         for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
-          if (!mbar_wait_cluster(&full[stage], phase, wd)) {
+          if (!ring_wait(&full[stage], phase, wd)) {
             ok = false;
             break;
           }
