@@ -163,6 +163,10 @@ static int64_t idle_split_pieces(int64_t k_blocks) {
   return p < 2 ? 2 : p;
 }
 
+// Short-K products the FMA kernel takes (see make_plan): K and output-size limits.
+constexpr int64_t kFmaMaxK = 24;
+constexpr int64_t kFmaMaxOutputs = int64_t{1} << 22;
+
 // Tile width by a wave-quantisation cost model: a persistent grid runs
 // ceil(tiles / slots) rounds, each as long as one tile. A 128-wide tile has half the
 // flops of a 256-wide one but, measured on GB300, takes about 0.8 of its time (0.74 on
@@ -215,6 +219,15 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   const bool f16acc = P.precision == GEMM_PREC_F16_ACC;
   pl.acc_chunk = f16acc ? (opt.acc_chunk > 0 ? opt.acc_chunk : kDefaultAccChunk) : 0;
   bool use_fma = (exact && P.M * P.N <= 256) || (f16acc && pl.acc_chunk % 16 != 0);
+  // A short K with a moderate output also takes the FMA kernel, unless a tensor-core tile
+  // shape is asked for: one launch that reads operands of any alignment, where the tensor
+  // cores need staging copies for misaligned rows and a launch whose fixed costs dominate.
+  // Replayed from CUDA graphs on GB300 (the 216 products of the ragged sweep, average per
+  // product): K = 1 4.5 against 8.8 us, K = 17 7.9 against 9.9, but K = 127 34 against
+  // 10 (the FMA kernel walks K serially in steps of 8).
+  const bool tile_asked = opt.cta_pair != 0 || opt.block_n != 0 || opt.stage_k != 0 ||
+                          opt.tile_rows != 0;
+  if (!tile_asked && P.K <= kFmaMaxK && P.M * P.N <= kFmaMaxOutputs) use_fma = true;
   if (opt.force_path == 2) use_fma = true;
   if (opt.force_path == 1) {
     if (f16acc && pl.acc_chunk % 16 != 0) return GEMM_ERR_UNSUPPORTED;

@@ -292,3 +292,16 @@ def test_plan_split_k_rule():
     # 2560^2: 256-wide tiles (128-wide ones cost 0.8 of a 256-wide one's time, too much
     # for the rounds they save)
     assert plan(2560, 2560, 8192, 152)["tile_n"] == 256
+
+
+def test_plan_short_k_takes_the_fma_kernel():
+    """A short K with a moderate output runs on the FMA kernel (one launch that reads any
+    alignment); a longer K, a large output, or a tensor-core tile asked for keeps the
+    tensor cores."""
+    f16 = torch.float16
+    assert g.plan(t((1000, 17), f16), t((17, 1000), f16), out_dtype="f32")["path"] == "fma"
+    assert g.plan(t((1025, 1), f16), t((1, 1025), f16), out_dtype="f32")["path"] == "fma"
+    assert g.plan(t((2048, 24), f16), t((24, 2048), f16), out_dtype="f32")["path"] == "fma"
+    assert g.plan(t((1000, 127), f16), t((127, 1000), f16), out_dtype="f32")["path"] == "tcgen05"
+    assert g.plan(t((1000, 25), f16), t((25, 1000), f16), out_dtype="f32")["path"] == "tcgen05"
+    assert g.plan(t((8192, 16), f16), t((16, 8192), f16), out_dtype="f32")["path"] == "tcgen05"
