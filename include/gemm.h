@@ -37,7 +37,8 @@
  * Precision (fp32 inputs only): GEMM_PREC_DEFAULT means GEMM_PREC_EXACT_FP32;
  * GEMM_PREC_TF32 runs the tensor cores on tf32 operands (the low 13 mantissa bits
  * of each fp32 input are ignored; max |err| <= 2e-3 * sum_k |a_ik b_kj|), reading
- * row- and column-major operands alike in place.
+ * row- and column-major operands alike in place (a product with a short K that the
+ * planner gives to the fp32 FMA kernel, see gemm_run_ex, is computed in full fp32).
  * GEMM_PREC_EXACT_FP32 keeps fp32 accuracy (max |err| <= 1e-6 * sum_k |a_ik b_kj|
  * on the library's tests): each operand is split into two tf32 parts and the
  * three significant partial products run on the tensor cores, accumulating in
@@ -128,8 +129,10 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
  * kernel -- the tcgen05 tensor-core kernels for 16-bit inputs and tf32 mode; for exact
  * fp32, the tensor cores on operands split once into tf32 hi and lo parts (three tf32
  * products, K summed in 128-long chunks in fp32 registers), or the fp32 FMA kernel for
- * problems too small to fill the tensor-core tiles -- stages misaligned operands, and
- * launches.
+ * problems too small to fill the tensor-core tiles; and the FMA kernel, for any input
+ * dtype, for a K of at most 24 with at most 2^22 outputs unless one of the tile options
+ * (GEMM_OPT_CTA_PAIR, BLOCK_N, STAGE_K, TILE_ROWS) is set -- stages misaligned operands,
+ * and launches.
  * Errors (nothing launched): INVALID_ARG for h == NULL, negative sizes, a null
  * pointer with a non-empty extent, a leading dimension below its minimum, an
  * unknown enum, or C's span overlapping A's or B's; UNSUPPORTED for a
@@ -236,7 +239,7 @@ typedef enum {
   GEMM_PATH_NONE = 0,      /* nothing to do (M == 0 or N == 0) */
   GEMM_PATH_ZERO_FILL = 1, /* K == 0: C is set to zero */
   GEMM_PATH_TCGEN05 = 2,   /* TMA + mbarrier pipeline + tcgen05.mma, TMEM accumulator */
-  GEMM_PATH_FMA = 3,       /* fp32 fused multiply-add tiles (exact fp32, tiny problems) */
+  GEMM_PATH_FMA = 3,       /* fp32 fused multiply-add tiles (tiny exact fp32, short K) */
   GEMM_PATH_TCGEN05_3XTF32 = 4, /* exact fp32 on the tensor cores: operands split into tf32
                                    hi/lo parts, three products in one fp32 accumulator */
   GEMM_PATH_TCGEN05_F16ACC = 5   /* fp16 accumulator on the tensor cores: each K-chunk's
@@ -308,7 +311,7 @@ typedef struct {
  * one of the candidates, so the choice is never slower as measured. Blocking: returns
  * after the last timing. It runs the real product, so C is written (with the product).
  * Problems that do not take the plain tensor-core path (exact fp32, the fp16 accumulator,
- * tiny or K = 0 problems) have a single candidate. `iters` in [1, 1000]. Different
+ * short-K, tiny or K = 0 problems) have a single candidate. `iters` in [1, 1000]. Different
  * choices sum in different orders: results stay within the precision bounds but may
  * differ in the last bits from the untuned plan. `result` may be NULL. */
 GEMM_API gemm_status_t gemm_tune(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
