@@ -58,12 +58,18 @@ __device__ __forceinline__ float f16_accumulate(float acc, float partial) {
   return __half2float(__float2half_rn(acc + h));
 }
 
+// The K-loop keeps two chunks of A and B in shared memory: while the threads multiply one,
+// the next chunk's elements are already on their way from global memory into registers and
+// go to the other buffer after the products, so a chunk's load latency overlaps the
+// previous chunk's arithmetic and each chunk needs one barrier.
 template <int BM, int BN, int BK, int TM, int TN, typename InT, bool F16ACC>
-__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+__global__ void __launch_bounds__((BM / TM) * (BN / TN),
+                                  (BM / TM) * (BN / TN) >= 256 && !F16ACC ? 2 : 1)
     fma_gemm_kernel(const FmaParams p) {
   constexpr int TX = BN / TN, TY = BM / TM, NT = TX * TY;
-  __shared__ float As[BK][BM];
-  __shared__ float Bs[BK][BN];
+  constexpr int LA = (BM * BK + NT - 1) / NT, LB = (BK * BN + NT - 1) / NT;  // loads a thread
+  __shared__ float As[2][BK][BM];
+  __shared__ float Bs[2][BK][BN];
   const int tid = threadIdx.x;
   const int tx = tid % TX, ty = tid / TX;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
@@ -82,38 +88,73 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
       for (int j = 0; j < TN; ++j) hacc[F16ACC ? i : 0][F16ACC ? j : 0] = 0.0f;
   }
 
+  // Element e of a chunk, walking each operand's contiguous axis fastest; zero outside
+  // rows < M, k < K, cols < N.
+  float ra[LA], rb[LB];
+  auto load_chunk = [&](int64_t k0) {
+#pragma unroll
+    for (int l = 0; l < LA; ++l) {
+      const int e = tid + l * NT;
+      float v = 0.0f;
+      if (e < BM * BK) {
+        const int r = p.a_col ? e % BM : e / BK;
+        const int kk = p.a_col ? e / BM : e % BK;
+        const int64_t i = m0 + r, k = k0 + kk;
+        if (i < p.M && k < p.K)
+          v = load_as_float<InT>(p.A, p.a_col ? k * p.lda + i : i * p.lda + k);
+      }
+      ra[l] = v;
+    }
+#pragma unroll
+    for (int l = 0; l < LB; ++l) {
+      const int e = tid + l * NT;
+      float v = 0.0f;
+      if (e < BK * BN) {
+        const int c = p.b_col ? e / BK : e % BN;
+        const int kk = p.b_col ? e % BK : e / BN;
+        const int64_t j = n0 + c, k = k0 + kk;
+        if (j < p.N && k < p.K)
+          v = load_as_float<InT>(p.B, p.b_col ? j * p.ldb + k : k * p.ldb + j);
+      }
+      rb[l] = v;
+    }
+  };
+  auto store_chunk = [&](int buf) {
+#pragma unroll
+    for (int l = 0; l < LA; ++l) {
+      const int e = tid + l * NT;
+      if (e < BM * BK) As[buf][p.a_col ? e / BM : e % BK][p.a_col ? e % BM : e / BK] = ra[l];
+    }
+#pragma unroll
+    for (int l = 0; l < LB; ++l) {
+      const int e = tid + l * NT;
+      if (e < BK * BN) Bs[buf][p.b_col ? e % BK : e / BN][p.b_col ? e / BK : e % BN] = rb[l];
+    }
+  };
+
+  load_chunk(0);
+  store_chunk(0);
+  __syncthreads();
+  int buf = 0;
   for (int64_t k0 = 0; k0 < p.K; k0 += BK) {
-    // A tile: rows m0.., k-columns k0..; walk the storage's contiguous axis fastest.
-    for (int e = tid; e < BM * BK; e += NT) {
-      const int r = p.a_col ? e % BM : e / BK;
-      const int kk = p.a_col ? e / BM : e % BK;
-      const int64_t i = m0 + r, k = k0 + kk;
-      float v = 0.0f;
-      if (i < p.M && k < p.K) v = load_as_float<InT>(p.A, p.a_col ? k * p.lda + i : i * p.lda + k);
-      As[kk][r] = v;
-    }
-    for (int e = tid; e < BK * BN; e += NT) {
-      const int c = p.b_col ? e / BK : e % BN;
-      const int kk = p.b_col ? e % BK : e / BN;
-      const int64_t j = n0 + c, k = k0 + kk;
-      float v = 0.0f;
-      if (j < p.N && k < p.K) v = load_as_float<InT>(p.B, p.b_col ? j * p.ldb + k : k * p.ldb + j);
-      Bs[kk][c] = v;
-    }
-    __syncthreads();
+    const bool more = k0 + BK < p.K;
+    if (more) load_chunk(k0 + BK);  // in flight during the products below
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[TM], b[TN];
 #pragma unroll
-      for (int i = 0; i < TM; ++i) a[i] = As[kk][owned<TM, BM>(ty, i)];
+      for (int i = 0; i < TM; ++i) a[i] = As[buf][kk][owned<TM, BM>(ty, i)];
 #pragma unroll
-      for (int j = 0; j < TN; ++j) b[j] = Bs[kk][owned<TN, BN>(tx, j)];
+      for (int j = 0; j < TN; ++j) b[j] = Bs[buf][kk][owned<TN, BN>(tx, j)];
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
+    // the other buffer was last read before the previous barrier
+    if (more) store_chunk(buf ^ 1);
     __syncthreads();
+    buf ^= 1;
     if (F16ACC && ((k0 + BK) % p.acc_chunk == 0 || k0 + BK >= p.K)) {  // chunk done
 #pragma unroll
       for (int i = 0; i < TM; ++i)
@@ -225,17 +266,21 @@ dim3 grid_2d(int64_t outer, int64_t inner, int threads) {
 
 }  // namespace
 
+// Tile kinds: 4 (the pages' 4 x 4 x 4 tiles), 8 (128 x 128 tiles, 8-long K-chunks: the
+// fp16 accumulator, whose chunks are multiples of 8) and 128 (128 x 128 tiles, 16-long
+// K-chunks: half the chunks, and barriers, over a long K).
 void fma_tile_shape(int tile, int *bm, int *bn, int *bk) {
   if (tile == 4) {
     *bm = 4, *bn = 4, *bk = 4;
   } else {
-    *bm = 128, *bn = 128, *bk = 8;
+    *bm = 128, *bn = 128, *bk = tile == 8 ? 8 : 16;
   }
 }
 
 cudaError_t fma_launch(const FmaParams &p, int tile, cudaStream_t s) {
   if (tile == 4) return fma_launch_tile<4, 4, 4, 1, 1>(p, s);
-  return fma_launch_tile<128, 128, 8, 8, 8>(p, s);
+  if (tile == 8) return fma_launch_tile<128, 128, 8, 8, 8>(p, s);
+  return fma_launch_tile<128, 128, 16, 8, 8>(p, s);
 }
 
 cudaError_t repack_launch(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,

@@ -235,7 +235,7 @@ gemm_status_t make_plan(const Problem &P, const Options &opt, int sm_count, Plan
   }
   const bool split = exact && !use_fma;
   if (use_fma) {
-    pl.fma_tile = (P.M * P.N <= 256 && !f16acc) ? 4 : 128;
+    pl.fma_tile = (P.M * P.N <= 256 && !f16acc) ? 4 : f16acc ? 8 : 128;
     int bm, bn, bk;
     fma_tile_shape(pl.fma_tile, &bm, &bn, &bk);
     if (pl.acc_chunk % bk) return GEMM_ERR_UNSUPPORTED;
