@@ -305,3 +305,22 @@ def test_plan_short_k_takes_the_fma_kernel():
     assert g.plan(t((1000, 127), f16), t((127, 1000), f16), out_dtype="f32")["path"] == "tcgen05"
     assert g.plan(t((1000, 25), f16), t((25, 1000), f16), out_dtype="f32")["path"] == "tcgen05"
     assert g.plan(t((8192, 16), f16), t((16, 8192), f16), out_dtype="f32")["path"] == "tcgen05"
+
+
+def test_plan_fma_tile_kinds():
+    """The FMA kernel's K-chunk: 4 for the pages' 4 x 4 x 4 tiles, 8 under the fp16
+    accumulator (whose chunks are multiples of 8, e.g. the pages' BLOCK_K = 8), 16 for the
+    other 128 x 128 tiles."""
+    f16, f32 = torch.float16, torch.float32
+    p = g.plan(t((1000, 17), f16), t((17, 1000), f16), out_dtype="f32")
+    assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (128, 128, 16)
+    assert p["k_iters"] == 2
+    p = g.plan(t((16, 16), f32), t((16, 16), f32), precision="exact")
+    assert p["path"] == "fma" and (p["tile_m"], p["tile_n"], p["tile_k"]) == (4, 4, 4)
+    # a short K under the fp16 accumulator: the FMA kernel with 8-long chunks
+    p = g.plan(t((64, 16), f16), t((16, 64), f16), out_dtype="f16", precision="f16acc")
+    assert p["path"] == "fma" and (p["tile_k"], p["k_iters"]) == (8, 2)
+    p = g.plan(t((64, 64), f16), t((64, 64), f16), out_dtype="f16", precision="f16acc")
+    assert p["path"] == "tcgen05_f16acc"
+    p = g.plan(t((8, 40), f16), t((40, 8), f16), out_dtype="f16", precision="f16acc")
+    assert p["path"] == "tcgen05_f16acc"  # K = 40 is past the short-K limit
