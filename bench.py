@@ -693,6 +693,14 @@ def roofline(p, bound, workload_name, kernel_ms, peaks, peak_src, sustained_peak
             "algorithmic_flops_per_launch": flops}
 
 
+def datasheet_peak(in_dtype, bound):
+    """The datasheet's dense peak for a product's input type, TFLOP/s: bf16/fp16 2250 (at
+    the 2070 MHz maximum clock), tf32 1100 for fp32 inputs, and a third of that for exact
+    fp32, which runs three tf32 products per fp32 product."""
+    ds = DATASHEET_BF16_TFLOPS * (TF32_OVER_BF16 if in_dtype == "f32" else 1.0)
+    return ds / 3.0 if bound == "tensor_x3" else ds
+
+
 def kernel_name(h, a, b, p):
     plan = h.plan(a, b, out_dtype=p.out_dtype, precision=p.precision)
     if plan["path"] == "tcgen05_3xtf32":
@@ -751,10 +759,7 @@ def measure_config(g, dev, name, peaks, peak_src, min_s=0.3, cpu_s=3.0, hot_l2=F
     if bound == "hbm":
         out["hbm_gbs"] = algorithmic_bytes(p) * n / (elapsed_ms / 1e3) / 1e9
     else:
-        # against the datasheet's dense peak for the input type (bf16 2250 TFLOP/s at the
-        # 2070 MHz maximum clock; tf32 1100; exact fp32 = three tf32 products)
-        ds = DATASHEET_BF16_TFLOPS * (TF32_OVER_BF16 if p.in_dtype == "f32" else 1.0)
-        ds /= 3.0 if bound == "tensor_x3" else 1.0
+        ds = datasheet_peak(p.in_dtype, bound)
         out["datasheet_peak_tflops"] = ds
         out["pct_of_datasheet_peak"] = 100.0 * out["value"] / ds
     if hot_l2:

@@ -69,3 +69,17 @@ def test_clock_summary_bins_and_loaded_filter():
 def test_percentiles():
     p = bench.percentiles([5.0, 1.0, 2.0, 4.0, 3.0, 6.0, 7.0, 8.0, 9.0, 10.0])
     assert (p["min"], p["median"], p["p90"], p["mean"], p["n"]) == (1.0, 5.5, 9.0, 5.5, 10)
+
+
+def test_datasheet_peaks_and_kernel_duration():
+    # the percentage of the datasheet peak each config line carries: bf16 2250 TFLOP/s,
+    # tf32 1100, exact fp32 (three tf32 products) 1100 / 3
+    assert bench.datasheet_peak("bf16", "tensor") == 2250.0
+    assert abs(bench.datasheet_peak("f32", "tensor") - 1100.0) < 1e-9
+    assert abs(bench.datasheet_peak("f32", "tensor_x3") - 1100.0 / 3) < 1e-9
+    # a step that is the kernel alone is timed over the region; with staging copies in the
+    # step, the events around the kernel are used
+    ms, how = bench.kernel_duration(10.0, 20, 20, 0.7)
+    assert ms == 0.5 and "region" in how
+    ms, how = bench.kernel_duration(10.0, 20, 60, 0.4)
+    assert ms == 0.4 and "events" in how
