@@ -397,6 +397,12 @@ def plan_strided(a, b, out=None, out_dtype=None, precision="default", sm_count=1
     return info.as_dict(), sinfo.as_dict()
 
 
+# Stand-in address of C for a plan made without an output tensor: 16-byte aligned and
+# outside any process's address space, so the planner's check that C does not overlap A or
+# B cannot be set off by where A and B happen to live.
+_NO_C = 1 << 62
+
+
 def plan(a, b, out=None, out_dtype=None, precision="default", sm_count=148, handle=None,
          a_ptr=None, b_ptr=None, c_ptr=None, ldc=None):
     """Host-only planner query (works without a GPU); returns a dict.
@@ -413,7 +419,7 @@ def plan(a, b, out=None, out_dtype=None, precision="default", sm_count=148, hand
     if ldc is None:
         ldc = max(out.stride(0), N, 1) if out is not None else max(N, 1)
     if c_ptr is None:
-        c_ptr = out.data_ptr() if out is not None else 1 << 20
+        c_ptr = out.data_ptr() if out is not None else _NO_C
     info = PlanInfo()
     code = lib().gemm_plan(handle.handle if handle is not None else None, M, N, K,
                            ctypes.c_void_p(a.data_ptr() if a_ptr is None else a_ptr), lda,
